@@ -1,0 +1,98 @@
+"""Seeded, platform-independent synthetic inputs for attention workloads.
+
+This module only draws random numbers; it holds none of the attention
+arithmetic, so the CUDA path and the fp64 oracle can both be fed from it.
+
+Generator: SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom
+number generators", OOPSLA 2014) used as a counter-based stream -- output
+``e`` of stream ``(seed, tensor)`` is the SplitMix64 finaliser applied to
+``key + (e + 1) * GAMMA`` -- then the Box-Muller transform in fp64, rounded to
+fp32 and then to bf16 with round-to-nearest-even.  Only 64-bit integer
+arithmetic and IEEE fp64 are used, so an x86 host and an Arm host draw the
+same bits (up to a last-ulp libm difference in log/cos/sin that the fp32 and
+bf16 roundings almost always absorb).
+
+Streams: tensor ids Q=0, K=1, V=2, dO=3, key-padding lengths=4.  A workload
+with index ``k`` in the configuration list uses seed ``1000 + k``.
+"""
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+STREAM = {"Q": 0, "K": 1, "V": 2, "dO": 3, "kv_len": 4}
+SEED_BASE = 1000
+
+
+def _mix64(z):
+    """SplitMix64 output finaliser on a uint64 array (wrapping arithmetic)."""
+    z = z.copy()
+    z ^= z >> np.uint64(30)
+    z *= _M1
+    z ^= z >> np.uint64(27)
+    z *= _M2
+    z ^= z >> np.uint64(31)
+    return z
+
+
+def _stream_key(seed, stream):
+    with np.errstate(over="ignore"):
+        k = _mix64(np.array([np.uint64(seed) * GAMMA], dtype=np.uint64))
+        k = _mix64(k + np.uint64(stream) * _M2 + GAMMA)
+    return k[0]
+
+
+def uint64_stream(seed, stream, n, start=0):
+    """Outputs start .. start+n-1 of the counter-based stream (seed, stream)."""
+    key = _stream_key(seed, stream)
+    with np.errstate(over="ignore"):
+        ctr = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+        return _mix64(key + ctr * GAMMA)
+
+
+def normal_f64(seed, stream, n):
+    """n iid N(0,1) fp64 draws (Box-Muller on pairs of 53-bit uniforms)."""
+    npairs = (n + 1) // 2
+    u = uint64_stream(seed, stream, 2 * npairs)
+    scale = 1.0 / 9007199254740992.0  # 2^-53
+    u1 = ((u[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * scale  # (0, 1]
+    u2 = (u[1::2] >> np.uint64(11)).astype(np.float64) * scale          # [0, 1)
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = 2.0 * np.pi * u2
+    out = np.empty(2 * npairs, np.float64)
+    out[0::2] = r * np.cos(t)
+    out[1::2] = r * np.sin(t)
+    return out[:n]
+
+
+def f32_to_bf16_bits(x):
+    """Round fp32 values to bf16 (nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    with np.errstate(over="ignore"):
+        return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits):
+    """Exact widening of bf16 bit patterns to fp64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def normal_bf16_bits(seed, stream, shape):
+    """iid N(0,1) values rounded fp64 -> fp32 -> bf16, as uint16 bit patterns."""
+    n = int(np.prod(shape))
+    return f32_to_bf16_bits(normal_f64(seed, stream, n).astype(np.float32)).reshape(shape)
+
+
+def kv_lengths(seed, B, lo, hi):
+    """Per-sequence key lengths, uniform integers in [lo, hi] (int32 [B])."""
+    u = uint64_stream(seed, STREAM["kv_len"], B)
+    return (np.uint64(lo) + u % np.uint64(hi - lo + 1)).astype(np.int32)
+
+
+def attention_inputs(seed, B, H, N, d, with_dout=True):
+    """bf16 bit patterns of Q, K, V (and dO) for one workload, each [B,H,N,d]."""
+    names = ("Q", "K", "V", "dO") if with_dout else ("Q", "K", "V")
+    return {nm: normal_bf16_bits(seed, STREAM[nm], (B, H, N, d)) for nm in names}

@@ -1,0 +1,446 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU oracle of standard (materialised) attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness reference that the
+ * CUDA kernels are checked against.  Only the test suite, the smoke check and
+ * the CPU-baseline leg of the benchmark may load it; the product library
+ * never links, calls or falls back to it.  It shares no code, header, table
+ * or helper with the CUDA path.
+ *
+ * What it computes -- the definition of exact attention, written out:
+ *
+ *   "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ *    IO-Awareness" (abstract) and the apxml.com chapter "高效注意力算法实现
+ *   (FlashAttention)", section "FlashAttention：融合算子与分块处理": the tiled
+ *   method changes how attention is executed, not what it computes, so the
+ *   oracle is the standard computation with S = QK^T and P = softmax(S)
+ *   materialised (the same chapter's introduction, and the study notes
+ *   "FlashAttention学习笔记", sections "标准attention计算" and "标准Safe
+ *   softmax").
+ *
+ *   For one (batch b, head h), with rows q_i, k_j, v_j of Q, K, V (d wide):
+ *     s_ij = scale * sum_c q_ic k_jc
+ *     M(i) = { j : j < len_b  and (not causal or j <= i) }   (visible keys)
+ *     m_i  = max_{j in M(i)} s_ij
+ *     p_ij = exp(s_ij - m_i) / sum_{j' in M(i)} exp(s_ij' - m_i),  j in M(i)
+ *     p_ij = 0                                                   otherwise
+ *     o_i  = sum_j p_ij v_j
+ *     L_i  = m_i + ln sum_{j in M(i)} exp(s_ij - m_i)     (natural log)
+ *   An empty M(i) gives o_i = 0 and L_i = -inf.
+ *
+ *   Backward (the gradient of the above; the pages only say that the
+ *   backward pass recomputes the attention matrix from the stored softmax
+ *   statistics -- fmread.com summary, section 三.2 "反向传播优化"):
+ *     dV   = P^T dO
+ *     dP   = dO V^T
+ *     D_i  = sum_j p_ij dP_ij            (from P and dP, not from O)
+ *     dS   = P o (dP - D)                (o = elementwise)
+ *     dQ   = scale * dS K
+ *     dK   = scale * dS^T Q
+ *
+ * Memory: S and P are materialised for a panel of complete rows (all keys of
+ * each row), so every softmax is a plain two-pass safe softmax: no online
+ * rescaling appears here.  Tensors are contiguous [B, H, N, d] fp64; L and
+ * kv_len are [B, H, N] and [B].
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG 1
+#define ORACLE_ERR_NOMEM 2
+
+/* Is key j visible from query i? (the mask set M(i) above) */
+static int visible(int64_t i, int64_t j, int causal, int64_t len)
+{
+    return j < len && (!causal || j <= i);
+}
+
+static double dot(const double *a, const double *b, int d)
+{
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += a[c] * b[c];
+    return acc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* A tiny task pool: tasks 0..ntasks-1 are handed out to nthreads threads.  */
+
+typedef void (*task_fn)(void *ctx, int64_t task, int worker);
+
+typedef struct {
+    task_fn fn;
+    void *ctx;
+    int64_t ntasks;
+    int64_t next;
+    pthread_mutex_t lock;
+} pool_t;
+
+typedef struct {
+    pool_t *pool;
+    int worker;
+} worker_arg_t;
+
+static void *pool_worker(void *arg)
+{
+    worker_arg_t *wa = (worker_arg_t *)arg;
+    pool_t *p = wa->pool;
+    for (;;) {
+        pthread_mutex_lock(&p->lock);
+        int64_t t = p->next++;
+        pthread_mutex_unlock(&p->lock);
+        if (t >= p->ntasks) break;
+        p->fn(p->ctx, t, wa->worker);
+    }
+    return NULL;
+}
+
+static void run_pool(task_fn fn, void *ctx, int64_t ntasks, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > ntasks) nthreads = (int)(ntasks > 0 ? ntasks : 1);
+    pool_t p;
+    p.fn = fn;
+    p.ctx = ctx;
+    p.ntasks = ntasks;
+    p.next = 0;
+    pthread_mutex_init(&p.lock, NULL);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    worker_arg_t *wa = (worker_arg_t *)malloc(sizeof(worker_arg_t) * (size_t)nthreads);
+    for (int w = 0; w < nthreads; ++w) {
+        wa[w].pool = &p;
+        wa[w].worker = w;
+    }
+    for (int w = 1; w < nthreads; ++w) pthread_create(&th[w], NULL, pool_worker, &wa[w]);
+    pool_worker(&wa[0]);
+    for (int w = 1; w < nthreads; ++w) pthread_join(th[w], NULL);
+    pthread_mutex_destroy(&p.lock);
+    free(th);
+    free(wa);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Row panel of one head: S and P for rows [r0, r0+R) against all N keys.   */
+
+/* Fills s[r*N + j] = scale * q_i . k_j and p[r*N + j] = softmax over M(i);
+ * lse[r] = the row's logsumexp.  Entries outside M(i) get p = 0 (s is left at
+ * 0 there and never read). */
+static void panel_probs(const double *q, const double *k, int64_t N, int d,
+                        double scale, int causal, int64_t len, int64_t r0,
+                        int64_t R, double *s, double *p, double *lse)
+{
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t i = r0 + r;
+        double *srow = s + r * N;
+        double *prow = p + r * N;
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            if (visible(i, j, causal, len)) {
+                srow[j] = scale * dot(q + i * d, k + j * d, d);
+                if (srow[j] > mx) mx = srow[j];
+            } else {
+                srow[j] = 0.0;
+            }
+        }
+        if (mx == -INFINITY) { /* empty M(i) */
+            for (int64_t j = 0; j < N; ++j) prow[j] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (visible(i, j, causal, len)) {
+                prow[j] = exp(srow[j] - mx);
+                sum += prow[j];
+            } else {
+                prow[j] = 0.0;
+            }
+        }
+        for (int64_t j = 0; j < N; ++j) prow[j] /= sum;
+        lse[r] = mx + log(sum);
+    }
+}
+
+/* Panel height so that one fp64 N-wide panel matrix stays under ~32 MB. */
+static int64_t panel_rows(int64_t N)
+{
+    int64_t R = (int64_t)(32 << 20) / (8 * (N > 0 ? N : 1));
+    if (R < 1) R = 1;
+    if (R > N) R = N;
+    return R;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Forward over whole tensors.                                               */
+
+typedef struct {
+    const double *q, *k, *v;
+    int64_t H, N;
+    int d;
+    double scale;
+    int causal;
+    const int *kv_len;
+    double *o, *L;
+    int err;
+} fwd_ctx_t;
+
+static void fwd_task(void *vctx, int64_t bh, int worker)
+{
+    (void)worker;
+    fwd_ctx_t *c = (fwd_ctx_t *)vctx;
+    int64_t N = c->N;
+    int d = c->d;
+    int64_t b = bh / c->H;
+    int64_t len = c->kv_len ? c->kv_len[b] : N;
+    const double *q = c->q + bh * N * d, *k = c->k + bh * N * d, *v = c->v + bh * N * d;
+    double *o = c->o + bh * N * d, *L = c->L + bh * N;
+    int64_t R = panel_rows(N);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(R * N));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(R * N));
+    double *lse = (double *)malloc(sizeof(double) * (size_t)R);
+    if (!s || !p || !lse) {
+        c->err = ORACLE_ERR_NOMEM;
+        free(s); free(p); free(lse);
+        return;
+    }
+    for (int64_t r0 = 0; r0 < N; r0 += R) {
+        int64_t rr = (r0 + R <= N) ? R : N - r0;
+        panel_probs(q, k, N, d, c->scale, c->causal, len, r0, rr, s, p, lse);
+        for (int64_t r = 0; r < rr; ++r) {
+            int64_t i = r0 + r;
+            double *oi = o + i * d;
+            for (int c2 = 0; c2 < d; ++c2) oi[c2] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                double pij = p[r * N + j];
+                if (pij == 0.0) continue;
+                const double *vj = v + j * d;
+                for (int c2 = 0; c2 < d; ++c2) oi[c2] += pij * vj[c2];
+            }
+            L[i] = lse[r];
+        }
+    }
+    free(s); free(p); free(lse);
+}
+
+int oracle_attn_fwd(const double *q, const double *k, const double *v, int B, int H,
+                    int N, int d, double scale, int causal, const int *kv_len,
+                    double *o, double *L, int nthreads)
+{
+    if (!q || !k || !v || !o || !L || B < 0 || H < 0 || N < 0 || d < 1) return ORACLE_ERR_ARG;
+    fwd_ctx_t c = {q, k, v, H, N, d, scale, causal, kv_len, o, L, ORACLE_OK};
+    run_pool(fwd_task, &c, (int64_t)B * H, nthreads);
+    return c.err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward over whole tensors (one task per (b, h): no cross-task sums).    */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t H, N;
+    int d;
+    double scale;
+    int causal;
+    const int *kv_len;
+    double *dq, *dk, *dv;
+    int err;
+} bwd_ctx_t;
+
+static void bwd_task(void *vctx, int64_t bh, int worker)
+{
+    (void)worker;
+    bwd_ctx_t *c = (bwd_ctx_t *)vctx;
+    int64_t N = c->N;
+    int d = c->d;
+    int64_t b = bh / c->H;
+    int64_t len = c->kv_len ? c->kv_len[b] : N;
+    int64_t off = bh * N * d;
+    const double *q = c->q + off, *k = c->k + off, *v = c->v + off, *dout = c->dout + off;
+    double *dq = c->dq + off, *dk = c->dk + off, *dv = c->dv + off;
+    int64_t R = panel_rows(N);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(R * N));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(R * N));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(R * N));
+    double *lse = (double *)malloc(sizeof(double) * (size_t)R);
+    if (!s || !p || !dp || !lse) {
+        c->err = ORACLE_ERR_NOMEM;
+        free(s); free(p); free(dp); free(lse);
+        return;
+    }
+    memset(dk, 0, sizeof(double) * (size_t)(N * d));
+    memset(dv, 0, sizeof(double) * (size_t)(N * d));
+    for (int64_t r0 = 0; r0 < N; r0 += R) {
+        int64_t rr = (r0 + R <= N) ? R : N - r0;
+        panel_probs(q, k, N, d, c->scale, c->causal, len, r0, rr, s, p, lse);
+        for (int64_t r = 0; r < rr; ++r) {
+            int64_t i = r0 + r;
+            const double *doi = dout + i * d;
+            double *prow = p + r * N, *dprow = dp + r * N;
+            /* dP_ij = dO_i . v_j and D_i = sum_j p_ij dP_ij */
+            double Di = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                dprow[j] = visible(i, j, c->causal, len) ? dot(doi, v + j * d, d) : 0.0;
+                Di += prow[j] * dprow[j];
+            }
+            double *dqi = dq + i * d;
+            for (int c2 = 0; c2 < d; ++c2) dqi[c2] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                double pij = prow[j];
+                if (pij == 0.0) continue;
+                double dsij = pij * (dprow[j] - Di);
+                const double *kj = k + j * d;
+                const double *qi = q + i * d;
+                double *dkj = dk + j * d, *dvj = dv + j * d;
+                for (int c2 = 0; c2 < d; ++c2) {
+                    dqi[c2] += c->scale * dsij * kj[c2];
+                    dkj[c2] += c->scale * dsij * qi[c2];
+                    dvj[c2] += pij * doi[c2];
+                }
+            }
+        }
+    }
+    free(s); free(p); free(dp); free(lse);
+}
+
+int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
+                    int B, int H, int N, int d, double scale, int causal, const int *kv_len,
+                    double *dq, double *dk, double *dv, int nthreads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H < 0 || N < 0 || d < 1)
+        return ORACLE_ERR_ARG;
+    bwd_ctx_t c = {q, k, v, dout, H, N, d, scale, causal, kv_len, dq, dk, dv, ORACLE_OK};
+    run_pool(bwd_task, &c, (int64_t)B * H, nthreads);
+    return c.err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sampled outputs of ONE head (q, k, v, dout are [N, d] of that head).      */
+/* They follow the same definitions row by row; used where the whole result */
+/* would take the CPU too long.                                              */
+
+/* o_out[r*d..], L_out[r] for the listed query rows. */
+int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, int d,
+                    double scale, int causal, int len, int nrows, const int *rows,
+                    double *o_out, double *L_out)
+{
+    if (!q || !k || !v || !rows || !o_out || !L_out || N < 1 || d < 1) return ORACLE_ERR_ARG;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s || !p) { free(s); free(p); return ORACLE_ERR_NOMEM; }
+    for (int r = 0; r < nrows; ++r) {
+        int64_t i = rows[r];
+        if (i < 0 || i >= N) { free(s); free(p); return ORACLE_ERR_ARG; }
+        double lse;
+        panel_probs(q, k, N, d, scale, causal, len, i, 1, s, p, &lse);
+        for (int c = 0; c < d; ++c) o_out[(int64_t)r * d + c] = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (p[j] == 0.0) continue;
+            for (int c = 0; c < d; ++c) o_out[(int64_t)r * d + c] += p[j] * v[j * d + c];
+        }
+        L_out[r] = lse;
+    }
+    free(s); free(p);
+    return ORACLE_OK;
+}
+
+/* dq_out[r*d..] for the listed query rows (each dQ row needs only its own
+ * row of P and dP). */
+int oracle_bwd_dq_rows(const double *q, const double *k, const double *v, const double *dout,
+                       int N, int d, double scale, int causal, int len, int nrows,
+                       const int *rows, double *dq_out)
+{
+    if (!q || !k || !v || !dout || !rows || !dq_out || N < 1 || d < 1) return ORACLE_ERR_ARG;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s || !p || !dp) { free(s); free(p); free(dp); return ORACLE_ERR_NOMEM; }
+    for (int r = 0; r < nrows; ++r) {
+        int64_t i = rows[r];
+        if (i < 0 || i >= N) { free(s); free(p); free(dp); return ORACLE_ERR_ARG; }
+        double lse;
+        panel_probs(q, k, N, d, scale, causal, len, i, 1, s, p, &lse);
+        const double *doi = dout + i * d;
+        double Di = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            dp[j] = visible(i, j, causal, len) ? dot(doi, v + j * d, d) : 0.0;
+            Di += p[j] * dp[j];
+        }
+        double *dqi = dq_out + (int64_t)r * d;
+        for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (p[j] == 0.0) continue;
+            double ds = p[j] * (dp[j] - Di);
+            for (int c = 0; c < d; ++c) dqi[c] += scale * ds * k[j * d + c];
+        }
+    }
+    free(s); free(p); free(dp);
+    return ORACLE_OK;
+}
+
+/* dK and dV rows (keys) for the listed key indices.  Every query row's
+ * logsumexp and D_i are needed first; they are computed for all N rows. */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t N;
+    int d;
+    double scale;
+    int causal;
+    int64_t len;
+    double *lse, *D;
+} rowstat_ctx_t;
+
+static void rowstat_task(void *vctx, int64_t i, int worker)
+{
+    (void)worker;
+    rowstat_ctx_t *c = (rowstat_ctx_t *)vctx;
+    int64_t N = c->N;
+    int d = c->d;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s || !p) { free(s); free(p); c->lse[i] = NAN; return; }
+    double lse;
+    panel_probs(c->q, c->k, N, d, c->scale, c->causal, c->len, i, 1, s, p, &lse);
+    double Di = 0.0;
+    for (int64_t j = 0; j < N; ++j)
+        if (p[j] != 0.0) Di += p[j] * dot(c->dout + i * d, c->v + j * d, d);
+    c->lse[i] = lse;
+    c->D[i] = Di;
+    free(s); free(p);
+}
+
+int oracle_bwd_dkdv_cols(const double *q, const double *k, const double *v,
+                         const double *dout, int N, int d, double scale, int causal,
+                         int len, int ncols, const int *cols, double *dk_out,
+                         double *dv_out, int nthreads)
+{
+    if (!q || !k || !v || !dout || !cols || !dk_out || !dv_out || N < 1 || d < 1)
+        return ORACLE_ERR_ARG;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)N);
+    double *D = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!lse || !D) { free(lse); free(D); return ORACLE_ERR_NOMEM; }
+    rowstat_ctx_t rc = {q, k, v, dout, N, d, scale, causal, len, lse, D};
+    run_pool(rowstat_task, &rc, N, nthreads);
+    for (int64_t i = 0; i < N; ++i)
+        if (isnan(lse[i])) { free(lse); free(D); return ORACLE_ERR_NOMEM; }
+    for (int r = 0; r < ncols; ++r) {
+        int64_t j = cols[r];
+        if (j < 0 || j >= N) { free(lse); free(D); return ORACLE_ERR_ARG; }
+        double *dkj = dk_out + (int64_t)r * d, *dvj = dv_out + (int64_t)r * d;
+        for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+        for (int64_t i = 0; i < N; ++i) {
+            if (!visible(i, j, causal, len)) continue;
+            double pij = exp(scale * dot(q + i * d, k + j * d, d) - lse[i]);
+            double dpij = dot(dout + i * d, v + j * d, d);
+            double ds = pij * (dpij - D[i]);
+            for (int c = 0; c < d; ++c) {
+                dkj[c] += scale * ds * q[i * d + c];
+                dvj[c] += pij * dout[i * d + c];
+            }
+        }
+    }
+    free(lse); free(D);
+    return ORACLE_OK;
+}

@@ -1,0 +1,163 @@
+"""ctypes access to the fp64 CPU oracle (``attn_oracle.c``) -- TEST INFRASTRUCTURE.
+
+The oracle is the plain definition of attention with S and P materialised,
+computed in fp64 on the host (see the header of ``attn_oracle.c`` for the
+formulas and the page sections they follow).  Only the test suite, the smoke
+check and the benchmark's CPU-baseline leg may use it.
+
+Inputs are numpy float64 arrays, contiguous ``[B, H, N, d]``; bf16 inputs are
+widened exactly by the caller before they reach this module.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile attn_oracle.c into liboracle.so (plain gcc, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def default_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        i, d = ctypes.c_int, ctypes.c_double
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, i, i, i, i, d, i, ip, dp, dp, i]
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, d, i, ip, dp, dp, dp, i]
+        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, i, i, d, i, i, i, ip, dp, dp]
+        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, ip, dp]
+        lib.oracle_bwd_dkdv_cols.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, ip, dp, dp, i]
+        for f in ("oracle_attn_fwd", "oracle_attn_bwd", "oracle_fwd_rows",
+                  "oracle_bwd_dq_rows", "oracle_bwd_dkdv_cols"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _i32(a):
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise RuntimeError("oracle %s failed with code %d" % (name, rc))
+
+
+def attn_fwd(q, k, v, scale, causal=False, kv_len=None, nthreads=None):
+    """Standard attention forward.  Returns (O [B,H,N,d], L [B,H,N]) in fp64."""
+    lib = _load()
+    B, H, N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    o = np.empty((B, H, N, d), np.float64)
+    L = np.empty((B, H, N), np.float64)
+    if kv_len is not None:
+        kv, kvp = _i32(kv_len)
+    else:
+        kv, kvp = None, None
+    rc = lib.oracle_attn_fwd(qp, kp, vp, B, H, N, d, float(scale), int(bool(causal)), kvp,
+                             _f64(o)[1], _f64(L)[1], int(nthreads or default_threads()))
+    _check(rc, "attn_fwd")
+    return o, L
+
+
+def attn_bwd(q, k, v, dout, scale, causal=False, kv_len=None, nthreads=None):
+    """Gradients of standard attention.  Returns (dQ, dK, dV), fp64 [B,H,N,d]."""
+    lib = _load()
+    B, H, N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    dout, dop = _f64(dout)
+    dq = np.empty((B, H, N, d), np.float64)
+    dk = np.empty((B, H, N, d), np.float64)
+    dv = np.empty((B, H, N, d), np.float64)
+    if kv_len is not None:
+        kv, kvp = _i32(kv_len)
+    else:
+        kv, kvp = None, None
+    rc = lib.oracle_attn_bwd(qp, kp, vp, dop, B, H, N, d, float(scale), int(bool(causal)), kvp,
+                             _f64(dq)[1], _f64(dk)[1], _f64(dv)[1],
+                             int(nthreads or default_threads()))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
+
+
+def fwd_rows(q, k, v, scale, causal, length, rows):
+    """O and L rows of ONE head (q, k, v are [N, d]) at the listed query rows."""
+    lib = _load()
+    N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    rows, rp = _i32(rows)
+    o = np.empty((len(rows), d), np.float64)
+    L = np.empty((len(rows),), np.float64)
+    rc = lib.oracle_fwd_rows(qp, kp, vp, N, d, float(scale), int(bool(causal)), int(length),
+                             len(rows), rp, _f64(o)[1], _f64(L)[1])
+    _check(rc, "fwd_rows")
+    return o, L
+
+
+def bwd_dq_rows(q, k, v, dout, scale, causal, length, rows):
+    """dQ rows of ONE head at the listed query rows."""
+    lib = _load()
+    N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    dout, dop = _f64(dout)
+    rows, rp = _i32(rows)
+    dq = np.empty((len(rows), d), np.float64)
+    rc = lib.oracle_bwd_dq_rows(qp, kp, vp, dop, N, d, float(scale), int(bool(causal)),
+                                int(length), len(rows), rp, _f64(dq)[1])
+    _check(rc, "bwd_dq_rows")
+    return dq
+
+
+def bwd_dkdv_cols(q, k, v, dout, scale, causal, length, cols, nthreads=None):
+    """dK and dV rows of ONE head at the listed key indices."""
+    lib = _load()
+    N, d = q.shape
+    q, qp = _f64(q)
+    k, kp = _f64(k)
+    v, vp = _f64(v)
+    dout, dop = _f64(dout)
+    cols, cp = _i32(cols)
+    dk = np.empty((len(cols), d), np.float64)
+    dv = np.empty((len(cols), d), np.float64)
+    rc = lib.oracle_bwd_dkdv_cols(qp, kp, vp, dop, N, d, float(scale), int(bool(causal)),
+                                  int(length), len(cols), cp, _f64(dk)[1], _f64(dv)[1],
+                                  int(nthreads or default_threads()))
+    _check(rc, "bwd_dkdv_cols")
+    return dk, dv
