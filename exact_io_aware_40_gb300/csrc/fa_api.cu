@@ -1,0 +1,246 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation, TMA
+// tensor-map encoding, the per-device error word, and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "kernels.h"
+
+namespace {
+
+// One error word per device, written by kernels that give up on a stalled
+// pipeline; read and cleared by fa_check_error.
+__device__ int g_fa_error_word;
+
+constexpr int kMaxDevices = 64;
+
+// Signature of the driver's cuTensorMapEncodeTiled (CUDA 12.0 ABI version).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+EncodeTiledFn g_encode = nullptr;
+
+fa_status current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Device address of this device's error word (cached per device).
+fa_status error_word(int dev, int** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return FA_OK;
+}
+
+fa_status encoder(EncodeTiledFn* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return FA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return FA_OK;
+}
+
+// Tensor map over a bf16 [BH, N, d] tensor, seen as 3-D (d, N, BH) with a
+// (64, rows, 1) box and 128-byte swizzle: one box is one 64-column atom of a
+// `rows`-row tile.  Rows past N of a head read as zero (and are not written),
+// so tiles never spill into the next head.
+fa_status map_bf16(EncodeTiledFn enc, CUtensorMap* m, const void* base, int d,
+                   int N, int BH, int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(N)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fa_status check_common(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const long long tiles = (static_cast<long long>(N) + 127) / 128;
+  if (tiles * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                       int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                       fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4) ||
+      (kv_len && !aligned(kv_len, 4)))
+    return FA_ERR_INVALID_ARG;
+  int dev;
+  if ((st = current_device(&dev)) != FA_OK) return st;
+  int* err;
+  if ((st = error_word(dev, &err)) != FA_OK) return st;
+  EncodeTiledFn enc;
+  if ((st = encoder(&enc)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if ((st = map_bf16(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &to, O, d, N, BH, 128)) != FA_OK) return st;
+  fa::FwdArgs a;
+  a.L = L;
+  a.kv_len = kv_len;
+  a.err = err;
+  a.H = H;
+  a.N = N;
+  a.BH = BH;
+  a.n_qtiles = (N + 127) / 128;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  if (fa::launch_fwd(d, tq, tk, tv, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                 int N, int d, float scale, int causal, fa_stream_t stream) {
+  return fa_fwd_kvlen(Q, K, V, O, L, B, H, N, d, scale, causal, nullptr, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                 float scale, int causal, const int32_t* kv_len, void* workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV || !workspace)
+    return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+      !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
+      !aligned(L, 16) || !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  int dev;
+  if ((st = current_device(&dev)) != FA_OK) return st;
+  int* err;
+  if ((st = error_word(dev, &err)) != FA_OK) return st;
+  EncodeTiledFn enc;
+  if ((st = encoder(&enc)) != FA_OK) return st;
+  const int BH = B * H;
+  const size_t rows = static_cast<size_t>(BH) * N;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         round256(rows * d * sizeof(float)));
+
+  fa::BwdPreArgs pre;
+  pre.O = static_cast<const uint16_t*>(O);
+  pre.dO = static_cast<const uint16_t*>(dO);
+  pre.D = Dvec;
+  pre.dq_acc = dq_acc;
+  pre.rows = static_cast<long long>(rows);
+  pre.d = d;
+  if (fa::launch_bwd_pre(pre, stream) != cudaSuccess) return FA_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = map_bf16(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tdo, dO, d, N, BH, 128)) != FA_OK) return st;
+  fa::BwdArgs a;
+  a.L = L;
+  a.D = Dvec;
+  a.dq_acc = dq_acc;
+  a.dK = static_cast<uint16_t*>(dK);
+  a.dV = static_cast<uint16_t*>(dV);
+  a.kv_len = kv_len;
+  a.err = err;
+  a.H = H;
+  a.N = N;
+  a.BH = BH;
+  a.n_ktiles = (N + 127) / 128;
+  a.n_qtiles = (N + 127) / 128;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  if (fa::launch_bwd(d, tq, tk, tv, tdo, a, stream) != cudaSuccess) return FA_ERR_CUDA;
+
+  fa::BwdPostArgs post;
+  post.dq_acc = dq_acc;
+  post.dQ = static_cast<uint16_t*>(dQ);
+  post.n = static_cast<long long>(rows) * d;
+  post.scale = scale;
+  if (fa::launch_bwd_post(post, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_check_error(fa_stream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  int dev;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  int* err;
+  if ((st = error_word(dev, &err)) != FA_OK) return st;
+  int host = 0;
+  if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (host != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return host == FA_ERR_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

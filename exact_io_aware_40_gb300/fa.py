@@ -1,0 +1,165 @@
+"""ctypes binding of the C ABI in include/fa.h (libfa_sm103.so).
+
+Argument marshalling only: every step of attention runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch provides device memory and
+streams); the library is loaded from this package directory and is never
+replaced by another implementation -- if it is missing or cannot load, calls
+raise.
+"""
+import ctypes
+import math
+import os
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_sm103.so")
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s returned %s" % (where, status_string(status)))
+
+
+def load_library():
+    """Load libfa_sm103.so (built by build.py); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("%s is not built; run exact_io_aware_40_gb300/build.py "
+                           "(or __graft_entry__.build())" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd_kvlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.fa_check_error.argtypes = [vp]
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_check_error"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load_library().fa_status_string(int(status)).decode()
+
+
+fa_status_string = status_string
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, ref):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(ref.device).cuda_stream)
+
+
+def _check(status, where):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    return tuple(int(x) for x in q.shape)
+
+
+def _expect(t, name, dtype, shape):
+    import torch
+    if t is None:
+        raise ValueError("%s is required" % name)
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != shape:
+        raise ValueError("%s must be a contiguous CUDA %s tensor of shape %s" % (name, dtype, shape))
+
+
+# ------------------------------------------------------------------ raw ABI
+
+def fa_fwd(q, k, v, o, L, scale, causal, stream=None):
+    """fa_fwd on torch tensors (bf16 [B,H,N,d] q/k/v/o, fp32 [B,H,N] L)."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d,
+                                 float(scale), int(bool(causal)), _stream(stream, q)), "fa_fwd")
+
+
+def fa_fwd_kvlen(q, k, v, o, L, scale, causal, kv_len, stream=None):
+    """fa_fwd_kvlen on torch tensors; kv_len is a CUDA int32 [B] tensor or None."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_fwd_kvlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d,
+                                       float(scale), int(bool(causal)), _ptr(kv_len),
+                                       _stream(stream, q)), "fa_fwd_kvlen")
+
+
+def fa_bwd_workspace_bytes(B, H, N, d):
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream=None):
+    """fa_bwd on torch tensors; workspace is a CUDA byte tensor."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                 _ptr(kv_len), _ptr(workspace), workspace.numel(),
+                                 _stream(stream, q)), "fa_bwd")
+
+
+def fa_check_error(stream=None, device=None):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device).cuda_stream
+    _check(load_library().fa_check_error(ctypes.c_void_p(int(stream))), "fa_check_error")
+
+
+# ------------------------------------------------------------------ convenience
+
+def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=None, stream=None):
+    """Exact attention forward.  Returns (O bf16 [B,H,N,d], L fp32 [B,H,N])."""
+    import torch
+    B, H, N, d = _shape(q)
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _expect(t, nm, torch.bfloat16, (B, H, N, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if kv_len is not None:
+        _expect(kv_len, "kv_len", torch.int32, (B,))
+    fa_fwd_kvlen(q, k, v, out, lse, scale, causal, kv_len, stream)
+    return out, lse
+
+
+def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, workspace=None,
+                  stream=None):
+    """Exact attention backward.  Returns (dQ, dK, dV), bf16 [B,H,N,d]."""
+    import torch
+    B, H, N, d = _shape(q)
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _expect(t, nm, torch.bfloat16, (B, H, N, d))
+    _expect(L, "L", torch.float32, (B, H, N))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if kv_len is not None:
+        _expect(kv_len, "kv_len", torch.int32, (B,))
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream)
+    return dq, dk, dv

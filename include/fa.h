@@ -1,0 +1,121 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa_sm103.so).
+ *
+ * The operation is exact scaled-dot-product attention computed by the tiled,
+ * IO-aware method ("FlashAttention: Fast and Memory-Efficient Exact Attention
+ * with IO-Awareness", abstract): Q is cut into blocks of B_r rows and K, V into
+ * blocks of B_c rows (study notes "FlashAttention学习笔记", section
+ * "分块计算整体流程(Tiling)"); each block product S_ij = Q_i K_j^T is masked and
+ * folded into a running softmax (apxml.com chapter "高效注意力算法实现
+ * (FlashAttention)", section "在线Softmax"), so that the N x N matrices S and P
+ * never reach device memory.  The result equals standard attention (same
+ * chapter, "FlashAttention不改变注意力的数学定义"):
+ *
+ *     O = softmax(scale * Q K^T + mask) V,     L = rowwise logsumexp (natural log)
+ *
+ * The backward pass recomputes P from L instead of reading a stored N x N
+ * matrix (fmread.com summary, section 三.2, "反向传播优化").
+ *
+ * Conventions shared by every entry point:
+ *   - Q, K, V, O, dO, dQ, dK, dV: bf16, contiguous [B, H, N, d] (d fastest),
+ *     DEVICE pointers, 16-byte aligned.  L and the workspace's statistics are
+ *     fp32; L is [B, H, N].
+ *   - d must be 64 or 128.  N >= 1, B >= 1, H >= 1, B*H*N*d < 2^31 per tensor
+ *     is NOT required (offsets are 64-bit), but N < 2^31.
+ *   - scale multiplies Q K^T before the mask and the softmax (usually 1/sqrt(d));
+ *     it must be finite and > 0.
+ *   - causal != 0 masks key j for query i when j > i (square attention,
+ *     diagonal kept).
+ *   - kv_len (optional, DEVICE int32 [B]): keys j >= kv_len[b] are masked for
+ *     every query of batch b; values are clamped to [0, N].  A query with no
+ *     visible key gets O = 0, L = -inf and zero gradients.
+ *   - Ownership: the caller owns every buffer.  The library allocates no device
+ *     memory in these calls; its only device state is one 4-byte error word per
+ *     device (a static device variable).
+ *   - Asynchrony: every call only enqueues work on `stream` (NULL = the legacy
+ *     default stream) and returns; nothing synchronises except
+ *     fa_check_error().
+ *   - Errors: invalid arguments return FA_ERR_INVALID_ARG (or
+ *     FA_ERR_UNSUPPORTED for a head dim or size the kernels do not handle) and
+ *     enqueue nothing.  A failed launch returns FA_ERR_CUDA.  A kernel that
+ *     detects a stalled pipeline gives up after a time limit, records
+ *     FA_ERR_TIMEOUT in the device error word and returns; fa_check_error()
+ *     reports it.  No C++ exception crosses this interface.
+ *   - Aliasing: outputs must not overlap inputs or each other.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_TIMEOUT = 4
+} fa_status;
+
+/*
+ * Forward pass (study notes "FlashAttention学习笔记", "Forward运作流程":
+ * S_ij = Q_i K_j^T, masked safe softmax, O_ij = P_ij V_j, with the running
+ * statistics of the online softmax).
+ *   Q, K, V  in : bf16 [B, H, N, d]
+ *   O       out : bf16 [B, H, N, d], rounded to nearest even
+ *   L       out : fp32 [B, H, N], L_i = ln sum_{j visible} exp(scale * q_i.k_j)
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                 int N, int d, float scale, int causal, fa_stream_t stream);
+
+/* Same as fa_fwd with per-batch key padding; kv_len may be NULL (= all N). */
+fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                       int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                       fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: an fp32 [B, H, N, d] accumulator for
+ * dQ plus the fp32 [B, H, N] row terms D_i = sum_c dO_ic O_ic, each region
+ * rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass: recomputes P = exp(scale * Q K^T - L) tile by tile (never
+ * storing it) and returns the gradients of sum(O * dO):
+ *   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dQ = scale dS K,
+ *   dK = scale dS^T Q,  with D_i = sum_c dO_ic O_ic.
+ *   Q, K, V, O, dO  in : bf16 [B, H, N, d]   (O and L from fa_fwd/fa_fwd_kvlen
+ *   L               in : fp32 [B, H, N]       with the same scale/mask)
+ *   dQ, dK, dV     out : bf16 [B, H, N, d]
+ *   workspace          : device, >= fa_bwd_workspace_bytes(B,H,N,d) bytes,
+ *                        256-byte aligned; contents on entry are ignored.
+ * Gradients with respect to L are not part of this interface.
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                 float scale, int causal, const int32_t* kv_len, void* workspace,
+                 size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word (FA_ERR_TIMEOUT if a kernel gave up), or FA_ERR_CUDA if the stream
+ * itself reports an error.
+ */
+fa_status fa_check_error(fa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

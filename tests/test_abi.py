@@ -1,0 +1,82 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point the
+header declares, and rejects invalid arguments on the host before touching
+the GPU (no compute call runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_40_gb300 import build as fab
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = fab.build()
+    from exact_io_aware_40_gb300 import fa
+    return fa.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(fa_[a-z0-9_]+)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_check_error",
+              "fa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from exact_io_aware_40_gb300 import fa
+    assert fa.status_string(0) == "FA_OK"
+    assert fa.status_string(4) == "FA_ERR_TIMEOUT"
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    from exact_io_aware_40_gb300 import fa
+    B, H, N, d = 2, 3, 100, 64
+    rows = B * H * N
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == r256(rows * d * 4) + r256(rows * 4)
+    assert fa.fa_bwd_workspace_bytes(B, H, N, 96) == 0
+    assert fa.fa_bwd_workspace_bytes(0, H, N, d) == 0
+
+
+def test_invalid_arguments_are_rejected_on_the_host(lib):
+    fake = ctypes.c_void_p(0x10000)        # 16-byte aligned, never dereferenced
+    odd = ctypes.c_void_p(0x10008)         # 8-byte aligned only
+    null = ctypes.c_void_p(0)
+    f = ctypes.c_float
+    # null pointer
+    assert lib.fa_fwd(null, fake, fake, fake, fake, 1, 1, 128, 64, f(0.125), 0, null) == 1
+    # unsupported head dim
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 128, 96, f(0.125), 0, null) == 2
+    # bad sizes and scale
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 0, 1, 128, 64, f(0.125), 0, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 0, 64, f(0.125), 0, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 128, 64, f(float("nan")), 0, null) == 1
+    assert lib.fa_fwd(fake, fake, fake, fake, fake, 1, 1, 128, 64, f(-1.0), 0, null) == 1
+    # misaligned tensor
+    assert lib.fa_fwd(odd, fake, fake, fake, fake, 1, 1, 128, 64, f(0.125), 0, null) == 1
+    # backward: short workspace, null gradient
+    args = [fake] * 9
+    assert lib.fa_bwd(*args, 1, 1, 128, 64, f(0.125), 0, null, fake, 16, null) == 1
+    args[6] = null
+    assert lib.fa_bwd(*args, 1, 1, 128, 64, f(0.125), 0, null, fake, 1 << 20, null) == 1

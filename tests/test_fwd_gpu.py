@@ -1,0 +1,121 @@
+"""GPU parity of the forward kernel against the fp64 oracle (through the C ABI).
+
+Whole-tensor comparisons where the oracle finishes in seconds (several
+128-row tiles, ragged tails, key padding, the BERT- and GPT-2-shaped
+workloads); sampled rows at the 16K-token sizes, in the same launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+import helpers as H
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from exact_io_aware_40_gb300 import build as fab, fa
+    fab.build()
+    return fa.load_library()
+
+
+def run_fwd(case, causal):
+    from exact_io_aware_40_gb300 import fa
+    o, L = fa.attention_fwd(case.dev["Q"], case.dev["K"], case.dev["V"], causal=causal,
+                            scale=case.scale, kv_len=case.kv_len_dev)
+    fa.fa_check_error()
+    return H.to_f64(o), H.to_f64(L)
+
+
+def check_full(case, causal):
+    o, L = run_fwd(case, causal)
+    o_ref, L_ref = oracle.attn_fwd(case.f64["Q"], case.f64["K"], case.f64["V"], case.scale,
+                                   causal, kv_len=case.kv_len)
+    eo, el = H.err_o(o, o_ref), H.err_l(L, L_ref)
+    assert eo <= H.TOL_O_ABS, ("O", eo)
+    assert el <= H.TOL_L_ABS, ("L", el)
+    return eo, el
+
+
+def check_rows(case, causal, heads, rows):
+    o, L = run_fwd(case, causal)
+    worst_o = worst_l = 0.0
+    for (b, h) in heads:
+        qh, kh, vh = (case.f64[n][b, h] for n in ("Q", "K", "V"))
+        o_ref, L_ref = oracle.fwd_rows(qh, kh, vh, case.scale, causal, case.length(b), rows)
+        worst_o = max(worst_o, H.err_o(o[b, h, rows], o_ref))
+        worst_l = max(worst_l, H.err_l(L[b, h, rows], L_ref))
+    assert worst_o <= H.TOL_O_ABS, ("O", worst_o)
+    assert worst_l <= H.TOL_L_ABS, ("L", worst_l)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_config(causal):
+    # B=1, H=2, N=128, d=64 (the tiny exact-check workload)
+    check_full(H.Case(1000, 1, 2, 128, 64), causal)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 2, 63, 127, 129, 200, 383, 520])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(d, N, causal):
+    check_full(H.Case(2000 + N, 2, 2, N, d), causal)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding_edges(d, causal):
+    # empty rows (length 0), a single key, a tail crossing a tile, full length
+    case = H.Case(3000, 4, 2, 300, d)
+    case.set_kv_len([0, 1, 129, 300])
+    o, L = run_fwd(case, causal)
+    o_ref, L_ref = oracle.attn_fwd(case.f64["Q"], case.f64["K"], case.f64["V"], case.scale,
+                                   causal, kv_len=case.kv_len)
+    assert np.all(o[0] == 0.0) and np.all(np.isneginf(L[0]))
+    assert H.err_o(o, o_ref) <= H.TOL_O_ABS
+    assert H.err_l(L, L_ref) <= H.TOL_L_ABS
+
+
+def test_bert_large_shaped():
+    # B=16, H=16, N=512, d=64, per-sequence key lengths uniform in [256, 512]
+    check_full(H.Case(1001, 16, 16, 512, 64, kv_range=(256, 512)), False)
+
+
+def test_gpt2_shaped():
+    # B=8, H=12, N=1024, d=64, causal
+    check_full(H.Case(1002, 8, 12, 1024, 64), True)
+
+
+LONG_ROWS = np.array([0, 1, 2, 127, 128, 129, 4095, 8191, 8192, 12345, 16254, 16255, 16256,
+                      16382, 16383])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_sampled_rows(causal):
+    # B=1, H=16, N=16384, d=128 -- sampled rows of three heads
+    case = H.Case(1003, 1, 16, 16384, 128)
+    check_rows(case, causal, [(0, 0), (0, 7), (0, 15)], LONG_ROWS)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [512, 1024, 2048, 4096, 8192, 16384])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sweep_sampled_rows(d, N, causal):
+    # fixed 16K tokens per batch: B = 16384 / N, H = 2048 / d
+    B, Hh = 16384 // N, 2048 // d
+    case = H.Case(1004, B, Hh, N, d, with_dout=False)
+    rows = np.unique(np.array([0, 1, N // 2 - 1, N // 2, N - 129, N - 128, N - 1]))
+    check_rows(case, causal, [(0, 0), (B - 1, Hh - 1)], rows)
+
+
+def test_deterministic():
+    case = H.Case(1005, 2, 4, 700, 128)
+    o1, L1 = run_fwd(case, True)
+    o2, L2 = run_fwd(case, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(L1, L2)
