@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Throughput of exact attention (forward + backward) on GB300, in TFLOP/s.
+
+One step = the whole hot path over one batch of the long-sequence workload
+(B=1, H=16, N=16384, d=128, bf16, iid N(0,1) inputs from the seeded
+generator): for causal = 0 and 1, the forward pass (fa_fwd) and the three
+backward stages (fa_bwd_prepare, fa_bwd_main, fa_bwd_finish).
+
+FLOPs are counted over the unmasked (query, key) pairs P of each pass:
+forward 4*d*P (QK^T and PV), backward 10*d*P (QK^T recomputed, dP, dV, dK,
+dQ); non-causal P = B*H*N^2, causal P = B*H*N(N+1)/2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+replicas, no collective on the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+B, H, N, D = 1, 16, 16384, 128
+SEED = 1003  # the long-sequence workload's seed
+WORKLOAD = "long-sequence attention B=1 H=16 N=16384 d=128 bf16, fwd+bwd, causal=0 and causal=1"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+# DRAM traffic of one fa_bwd_main launch on this workload (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
+# launches), valid only while the kernel source hashes to the recorded digest.
+BWD_MAIN_TRAFFIC = {"sha256": None, "bytes_per_launch": None}
+
+
+def pairs(causal, b=B, h=H, n=N):
+    return b * h * (n * (n + 1) // 2 if causal else n * n)
+
+
+def step_flops(b=B, h=H, n=N, d=D):
+    return sum(14 * d * pairs(c, b, h, n) for c in (0, 1))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_digest():
+    h = hashlib.sha256()
+    for name in ("fa_bwd.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "exact_io_aware_40_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm
+
+_BITS = {}
+
+
+def workload_bits():
+    """bf16 bit patterns of the workload's Q, K, V, dO (generated once)."""
+    if not _BITS:
+        from exact_io_aware_40_gb300 import inputs
+        _BITS.update(inputs.attention_inputs(SEED, B, H, N, D))
+    return _BITS
+
+
+def oracle_sample(n_sample, threads):
+    """Times the fp64 oracle (as it stands) on the first n_sample tokens of each
+    head of the workload, forward + backward, causal 0 and 1.  Returns (seconds,
+    FLOPs counted like the GPU's, sample description)."""
+    from exact_io_aware_40_gb300 import inputs
+    from oracle import oracle
+    f64 = {k: inputs.bf16_bits_to_f64(v[:, :, :n_sample]) for k, v in workload_bits().items()}
+    scale = 1.0 / math.sqrt(D)
+    t0 = time.perf_counter()
+    for c in (0, 1):
+        oracle.attn_fwd(f64["Q"], f64["K"], f64["V"], scale, c, nthreads=threads)
+        oracle.attn_bwd(f64["Q"], f64["K"], f64["V"], f64["dO"], scale, c, nthreads=threads)
+    secs = time.perf_counter() - t0
+    flops = step_flops(n=n_sample)
+    desc = ("first %d of %d tokens of each of the %d heads (same inputs), fwd+bwd, causal 0 and 1, "
+            "fp64" % (n_sample, N, H))
+    return secs, flops, desc
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    from oracle import oracle
+    oracle.build()
+    threads = cpu_threads()
+    n_sample = 1024
+    for _ in range(args.warmup):
+        oracle_sample(n_sample, threads)
+    secs_total, flops_total = 0.0, 0
+    desc = ""
+    for _ in range(args.steps):
+        s, f, desc = oracle_sample(n_sample, threads)
+        secs_total += s
+        flops_total += f
+    value = flops_total / secs_total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs_total / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": [0, 1],
+                   "passes": "fwd+bwd", "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from exact_io_aware_40_gb300 import build as fab, fa, inputs
+
+    fab.build()
+    fa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    scale = 1.0 / math.sqrt(D)
+    bits = workload_bits()
+    host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for k, v in bits.items()}
+    q, k, v, do = (host[n].to(dev) for n in ("Q", "K", "V", "dO"))
+    out = {}
+    for c in (0, 1):
+        out[c] = dict(o=torch.empty_like(q), L=torch.empty((B, H, N), dtype=torch.float32, device=dev),
+                      dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    stages = ("fwd", "prep", "main", "finish")
+
+    def step(ev=None):
+        for c in (0, 1):
+            t = out[c]
+            if ev is not None:
+                ev[c][0].record(stream)
+            fa.fa_fwd(q, k, v, t["o"], t["L"], scale, c, stream=sp)
+            if ev is not None:
+                ev[c][1].record(stream)
+            fa.fa_bwd_prepare(t["o"], do, ws, stream=sp)
+            if ev is not None:
+                ev[c][2].record(stream)
+            fa.fa_bwd_main(q, k, v, do, t["L"], t["dk"], t["dv"], scale, c, None, ws, stream=sp)
+            if ev is not None:
+                ev[c][3].record(stream)
+            fa.fa_bwd_finish(t["dq"], scale, ws, stream=sp)
+            if ev is not None:
+                ev[c][4].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    fa.fa_check_error(sp)
+    torch.cuda.synchronize()
+    barrier()
+
+    # ---- device-resident timed region
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in (0, 1)]
+           for _ in range(args.steps)]
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_uuid = dev.index
+    sampler = ClockSampler(gpu_uuid)
+    with sampler:
+        torch.cuda.synchronize()
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_stop = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    fa.fa_check_error(sp)
+    ms_total = t_start.elapsed_time(t_stop)
+    per_stage = {c: {st: 0.0 for st in stages} for c in (0, 1)}
+    for s in range(args.steps):
+        for c in (0, 1):
+            for i, st in enumerate(stages):
+                per_stage[c][st] += evs[s][c][i].elapsed_time(evs[s][c][i + 1])
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    flops = step_flops()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device, both passes, results -> pinned host
+    host_out = {c: {n: torch.empty(out[c][n].shape, dtype=out[c][n].dtype).pin_memory()
+                    for n in ("o", "L", "dq", "dk", "dv")} for c in (0, 1)}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ("Q", "K", "V", "dO"))
+    d2h = sum(t.numel() * t.element_size() for c in (0, 1) for t in host_out[c].values())
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for dst, nm in ((q, "Q"), (k, "K"), (v, "V"), (do, "dO")):
+            dst.copy_(host[nm], non_blocking=True)
+        step()
+        for c in (0, 1):
+            for n in ("o", "L", "dq", "dk", "dv"):
+                host_out[c][n].copy_(out[c][n], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    fa.fa_check_error(sp)
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    if rank != 0:
+        return
+
+    peaks, peak_src = load_peaks()
+    main_ms = sum(per_stage[c]["main"] for c in (0, 1)) / (2 * args.steps)
+    main_flops = sum(10 * D * pairs(c) for c in (0, 1)) / 2
+    achieved = main_flops / (main_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = None
+    if BWD_MAIN_TRAFFIC["sha256"] == kernel_digest():
+        traffic = BWD_MAIN_TRAFFIC["bytes_per_launch"]
+    fwd_ms = sum(per_stage[c]["fwd"] for c in (0, 1)) / args.steps
+    bwd_ms = sum(per_stage[c][st] for c in (0, 1) for st in ("prep", "main", "finish")) / args.steps
+
+    threads = cpu_threads()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        secs, cflops, desc = oracle_sample(2048, threads)
+        cpu = {"value": cflops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 2)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": [0, 1],
+                   "passes": "fwd+bwd", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (Q, K, V, dO, outputs: 64 MiB each; 128 MiB fp32 "
+                         "dQ accumulator) -- no flush between steps"},
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd_main (mean of causal 0/1 launches)",
+                     "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "traffic": traffic,
+                     "peak_source": "bf16_tflops_sustained of %s peaks" % peak_src,
+                     "frac_of_burst_peak": achieved / burst},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": 8 * args.steps,
+        "clocks": sampler.summary(),
+        "per_pass": {
+            "fwd_ms": fwd_ms, "fwd_tflops": sum(4 * D * pairs(c) for c in (0, 1)) / (fwd_ms * 1e-3) / 1e12,
+            "bwd_ms": bwd_ms,
+            "bwd_tflops": sum(10 * D * pairs(c) for c in (0, 1)) / (bwd_ms * 1e-3) / 1e12,
+            "stage_ms": {str(c): {st: per_stage[c][st] / args.steps for st in stages} for c in (0, 1)},
+        },
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the oracle on the host cores")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        # the reference arm is the host-side oracle: rank 0 only, no GPU work
+        run_reference(args, rank)
+        return
+    import torch
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

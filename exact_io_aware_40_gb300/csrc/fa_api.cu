@@ -158,19 +158,49 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                 float scale, int causal, const int32_t* kv_len, void* workspace,
-                 size_t workspace_bytes, fa_stream_t stream) {
-  if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV || !workspace)
-    return FA_ERR_INVALID_ARG;
+// Splits the workspace into the fp32 dQ accumulator and the fp32 D vector.
+static void workspace_parts(void* ws, int BH, int N, int d, float** dq_acc, float** Dvec) {
+  const size_t rows = static_cast<size_t>(BH) * N;
+  *dq_acc = static_cast<float*>(ws);
+  *Dvec = reinterpret_cast<float*>(static_cast<char*>(ws) + round256(rows * d * sizeof(float)));
+}
+
+static fa_status check_workspace(const void* ws, size_t bytes, int B, int H, int N, int d) {
+  if (!ws || !aligned(ws, 256)) return FA_ERR_INVALID_ARG;
+  if (bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status fa_bwd_prepare(const void* O, const void* dO, int B, int H, int N, int d,
+                         void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!O || !dO) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d, 1.f);
+  if (st != FA_OK) return st;
+  if (!aligned(O, 16) || !aligned(dO, 16)) return FA_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  float *dq_acc, *Dvec;
+  workspace_parts(workspace, B * H, N, d, &dq_acc, &Dvec);
+  fa::BwdPreArgs pre;
+  pre.O = static_cast<const uint16_t*>(O);
+  pre.dO = static_cast<const uint16_t*>(dO);
+  pre.D = Dvec;
+  pre.dq_acc = dq_acc;
+  pre.rows = static_cast<long long>(B) * H * N;
+  pre.d = d;
+  return fa::launch_bwd_pre(pre, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+                      const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream) {
+  if (!Q || !K || !V || !dO || !L || !dK || !dV) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
-  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
-      !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
-      !aligned(L, 16) || !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) ||
+      !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
-  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
   int dev;
   if ((st = current_device(&dev)) != FA_OK) return st;
   int* err;
@@ -178,20 +208,8 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   EncodeTiledFn enc;
   if ((st = encoder(&enc)) != FA_OK) return st;
   const int BH = B * H;
-  const size_t rows = static_cast<size_t>(BH) * N;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         round256(rows * d * sizeof(float)));
-
-  fa::BwdPreArgs pre;
-  pre.O = static_cast<const uint16_t*>(O);
-  pre.dO = static_cast<const uint16_t*>(dO);
-  pre.D = Dvec;
-  pre.dq_acc = dq_acc;
-  pre.rows = static_cast<long long>(rows);
-  pre.d = d;
-  if (fa::launch_bwd_pre(pre, stream) != cudaSuccess) return FA_ERR_CUDA;
-
+  float *dq_acc, *Dvec;
+  workspace_parts(workspace, BH, N, d, &dq_acc, &Dvec);
   CUtensorMap tq, tk, tv, tdo;
   if ((st = map_bf16(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
   if ((st = map_bf16(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
@@ -213,15 +231,45 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
-  if (fa::launch_bwd(d, tq, tk, tv, tdo, a, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return fa::launch_bwd(d, tq, tk, tv, tdo, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
+fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream) {
+  if (!dQ) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned(dQ, 16)) return FA_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  float *dq_acc, *Dvec;
+  workspace_parts(const_cast<void*>(workspace), B * H, N, d, &dq_acc, &Dvec);
   fa::BwdPostArgs post;
   post.dq_acc = dq_acc;
   post.dQ = static_cast<uint16_t*>(dQ);
-  post.n = static_cast<long long>(rows) * d;
+  post.n = static_cast<long long>(B) * H * N * d;
   post.scale = scale;
-  if (fa::launch_bwd_post(post, stream) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+  return fa::launch_bwd_post(post, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                 float scale, int causal, const int32_t* kv_len, void* workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV || !workspace)
+    return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+      !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
+      !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
+    return FA_ERR_INVALID_ARG;
+  if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  if ((st = fa_bwd_prepare(O, dO, B, H, N, d, workspace, workspace_bytes, stream)) != FA_OK)
+    return st;
+  if ((st = fa_bwd_main(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, workspace,
+                        workspace_bytes, stream)) != FA_OK)
+    return st;
+  return fa_bwd_finish(dQ, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_check_error(fa_stream_t stream) {

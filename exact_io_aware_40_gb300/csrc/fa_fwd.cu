@@ -108,8 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x / a.BH);  // heavy tiles first
-  const int bh = static_cast<int>(blockIdx.x % a.BH);
+  // Head-major order: the CTAs in flight share one head's K/V (L2 reuse); within
+  // a head the longest query blocks (causal) start first.
+  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
+  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
   const int q0 = qt * kBR;
   const int b = bh / a.H;
   int kv_limit = a.N;
@@ -264,17 +266,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key >= kv_limit || (a.causal && key > grow)) sr[c][e] = __float_as_uint(-INFINITY);
           }
       }
-      float mx = -INFINITY;
+      // Row max as a tree (independent partial maxima, no long dependency chain).
+      float mxp[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mxp[t] = __uint_as_float(sr[0][t]);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        for (int e = (c == 0 ? 8 : 0); e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(sr[c][e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       const float m_cand = fmaxf(m_run, mx * a.scale_log2);
       const bool grow_max = m_cand > m_run + kRescaleThreshold;
       const float m_new = grow_max ? m_cand : m_run;
       const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float sum = 0.f;
+      float sp[4] = {0.f, 0.f, 0.f, 0.f};  // partial row sums
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -282,22 +289,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), a.scale_log2, -m_use));
           const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), a.scale_log2, -m_use));
-          sum += p0 + p1;
+          sp[e & 3] += p0 + p1;
           pk[e] = pack_bf16(p0, p1);
         }
         // P occupies the first 64 columns of the S buffer (2 bf16 per column).
         tmem_st16(tl + s_col(bb) + 16 * c, pk);
       }
-      l_run = l_run * alpha + sum;
+      l_run = l_run * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
       m_run = m_new;
-      if (j > 0) {
-        // O holds P_0..P_{j-1} V; rescale it once PV_{j-1} has landed.
+      if (j > 0 && __any_sync(0xffffffffu, grow_max)) {
+        // O holds P_0..P_{j-1} V; rescale it once PV_{j-1} has landed.  (Only
+        // PV_{j-1} can be pending: PV_{j-2} completed before S_j was issued, so
+        // the parity of this wait is unambiguous even when earlier ones were
+        // skipped.)
         if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, ab))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, grow_max)) {
+        {
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t o[32];

@@ -65,7 +65,7 @@ __device__ __forceinline__ void raise_timeout(Abort a) {
 // Waits for the phase with the given parity to complete.  Gives up (and
 // returns false) when the time limit passes, when another role of this CTA
 // gave up, or when another CTA recorded an error.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a) {
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
@@ -85,7 +85,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a) {
 }
 
 // Same, without an abort context: only for drain waits during unwinding.
-__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer() - t0 > kWaitLimitNs) return false;

@@ -42,10 +42,14 @@ def load_library():
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.fa_bwd_prepare.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
+    lib.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.fa_bwd_finish.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
     lib.fa_check_error.argtypes = [vp]
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
-    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_check_error"):
+    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_main",
+               "fa_bwd_finish", "fa_check_error"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -116,6 +120,29 @@ def fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stre
                                  _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                                  _ptr(kv_len), _ptr(workspace), workspace.numel(),
                                  _stream(stream, q)), "fa_bwd")
+
+
+def fa_bwd_prepare(o, do, workspace, stream=None):
+    """fa_bwd_prepare: D = rowsum(dO * O) and a zeroed dQ accumulator in workspace."""
+    B, H, N, d = _shape(o)
+    _check(load_library().fa_bwd_prepare(_ptr(o), _ptr(do), B, H, N, d, _ptr(workspace),
+                                         workspace.numel(), _stream(stream, o)), "fa_bwd_prepare")
+
+
+def fa_bwd_main(q, k, v, do, L, dk, dv, scale, causal, kv_len, workspace, stream=None):
+    """fa_bwd_main: dK, dV, and dS K added into the workspace's dQ accumulator."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(dk),
+                                      _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                      _ptr(kv_len), _ptr(workspace), workspace.numel(),
+                                      _stream(stream, q)), "fa_bwd_main")
+
+
+def fa_bwd_finish(dq, scale, workspace, stream=None):
+    """fa_bwd_finish: dQ = bf16(scale * accumulator)."""
+    B, H, N, d = _shape(dq)
+    _check(load_library().fa_bwd_finish(_ptr(dq), B, H, N, d, float(scale), _ptr(workspace),
+                                        workspace.numel(), _stream(stream, dq)), "fa_bwd_finish")
 
 
 def fa_check_error(stream=None, device=None):

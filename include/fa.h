@@ -20,8 +20,8 @@
  *   - Q, K, V, O, dO, dQ, dK, dV: bf16, contiguous [B, H, N, d] (d fastest),
  *     DEVICE pointers, 16-byte aligned.  L and the workspace's statistics are
  *     fp32; L is [B, H, N].
- *   - d must be 64 or 128.  N >= 1, B >= 1, H >= 1, B*H*N*d < 2^31 per tensor
- *     is NOT required (offsets are 64-bit), but N < 2^31.
+ *   - d must be 64 or 128; B, H, N >= 1; B*H*ceil(N/128) < 2^31 (element
+ *     offsets are 64-bit, so tensors may exceed 2^31 elements).
  *   - scale multiplies Q K^T before the mask and the softmax (usually 1/sqrt(d));
  *     it must be finite and > 0.
  *   - causal != 0 masks key j for query i when j > i (square attention,
@@ -103,6 +103,25 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
                  float scale, int causal, const int32_t* kv_len, void* workspace,
                  size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * The three stages fa_bwd enqueues, for callers that want to schedule or time
+ * them separately.  Arguments mean the same as in fa_bwd; each validates its
+ * own arguments.  fa_bwd == fa_bwd_prepare; fa_bwd_main; fa_bwd_finish.
+ *   fa_bwd_prepare: D_i = sum_c dO_ic O_ic into the workspace and zeroes the
+ *                   workspace's fp32 dQ accumulator (HBM-bound).
+ *   fa_bwd_main:    the recompute kernel: writes dK, dV and adds dS K into the
+ *                   workspace's dQ accumulator.  Needs a prepared workspace.
+ *   fa_bwd_finish:  dQ = bf16(scale * accumulator) (HBM-bound).
+ */
+fa_status fa_bwd_prepare(const void* O, const void* dO, int B, int H, int N, int d,
+                         void* workspace, size_t workspace_bytes, fa_stream_t stream);
+fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+                      const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream);
+fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's error
