@@ -10,6 +10,7 @@
 
 #include "fa.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -97,9 +98,37 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// A pipeline stage whose producer never arrives: every thread of one CTA waits
+// on an mbarrier that nothing signals, through the same bounded wait the
+// attention kernels use, and must give up after `limit_ns`.
+__global__ void stalled_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int flag;
+  if (threadIdx.x == 0) {
+    fa::mbar_init(fa::smem_u32(&bar), 1);
+    flag = 0;
+    fa::fence_mbar_init();
+  }
+  __syncthreads();
+  const fa::Abort ab{err, &flag};
+  fa::mbar_wait(fa::smem_u32(&bar), 0, ab, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_selftest_stalled_wait(uint64_t limit_ns, fa_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  int dev;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  int* err;
+  if ((st = error_word(dev, &err)) != FA_OK) return st;
+  stalled_wait_kernel<<<1, 64, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 const char* fa_status_string(fa_status s) {
   switch (s) {

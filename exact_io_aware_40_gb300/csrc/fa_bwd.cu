@@ -389,9 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     ok = bar_and(1, 128, ok && *abort_flag == 0);
-    if (ok && key < a.N) {
+    if (ok) {
       // ------------------------------------------------------------ dK, dV rows
-      const long long row = static_cast<long long>(bh) * a.N + key;
+      // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
+      const bool store = key < a.N;
+      const long long row = static_cast<long long>(bh) * a.N + (store ? key : 0);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         uint16_t* dst = (which == 0 ? a.dV : a.dK) + row * HD;
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.y = pack_bf16(__uint_as_float(r[8 * t + 2]) * mul, __uint_as_float(r[8 * t + 3]) * mul);
             v.z = pack_bf16(__uint_as_float(r[8 * t + 4]) * mul, __uint_as_float(r[8 * t + 5]) * mul);
             v.w = pack_bf16(__uint_as_float(r[8 * t + 6]) * mul, __uint_as_float(r[8 * t + 7]) * mul);
-            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * t) = v;
+            if (store) *reinterpret_cast<uint4*>(dst + 32 * c + 8 * t) = v;
           }
         }
       }

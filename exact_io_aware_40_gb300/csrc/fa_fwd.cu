@@ -269,11 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Row max as a tree (independent partial maxima, no long dependency chain).
       float mxp[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mxp[t] = __uint_as_float(sr[0][t]);
+      for (int t = 0; t < 8; ++t) mxp[t] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = (c == 0 ? 8 : 0); e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(sr[c][e]));
+        for (int e = 0; e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(sr[c][e]));
       const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                              fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       const float m_cand = fmaxf(m_run, mx * a.scale_log2);

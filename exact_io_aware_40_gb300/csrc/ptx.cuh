@@ -62,13 +62,18 @@ __device__ __forceinline__ void raise_timeout(Abort a) {
   atomicCAS(a.err, kErrNone, kErrTimeout);
 }
 
+// Second bound on every wait, independent of the clock: at most this many
+// rounds of 32 polls (each poll may suspend the thread for a short while).
+constexpr uint32_t kMaxWaitRounds = 1u << 20;
+
 // Waits for the phase with the given parity to complete.  Gives up (and
 // returns false) when the time limit passes, when another role of this CTA
 // gave up, or when another CTA recorded an error.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a) {
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a,
+                                              uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (;;) {
+  for (uint32_t round = 0;; ++round) {
 #pragma unroll 1
     for (int k = 0; k < 32; ++k)
       if (mbar_try_wait(bar, parity)) return true;
@@ -77,7 +82,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abo
       *a.flag = 1;
       return false;
     }
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns || round >= kMaxWaitRounds) {
       raise_timeout(a);
       return false;
     }
@@ -87,8 +92,8 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abo
 // Same, without an abort context: only for drain waits during unwinding.
 static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  for (uint32_t round = 0; !mbar_try_wait(bar, parity); ++round)
+    if (globaltimer() - t0 > kWaitLimitNs || round >= 32u * kMaxWaitRounds) return false;
   return true;
 }
 

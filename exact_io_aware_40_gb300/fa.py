@@ -45,11 +45,12 @@ def load_library():
     lib.fa_bwd_prepare.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
     lib.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.fa_bwd_finish.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_selftest_stalled_wait.argtypes = [ctypes.c_uint64, vp]
     lib.fa_check_error.argtypes = [vp]
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_main",
-               "fa_bwd_finish", "fa_check_error"):
+               "fa_bwd_finish", "fa_check_error", "fa_selftest_stalled_wait"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -143,6 +144,15 @@ def fa_bwd_finish(dq, scale, workspace, stream=None):
     B, H, N, d = _shape(dq)
     _check(load_library().fa_bwd_finish(_ptr(dq), B, H, N, d, float(scale), _ptr(workspace),
                                         workspace.numel(), _stream(stream, dq)), "fa_bwd_finish")
+
+
+def fa_selftest_stalled_wait(limit_ns, stream=None):
+    """Enqueue the stalled-wait self test; fa_check_error then reports FA_ERR_TIMEOUT."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(load_library().fa_selftest_stalled_wait(int(limit_ns), ctypes.c_void_p(int(stream))),
+           "fa_selftest_stalled_wait")
 
 
 def fa_check_error(stream=None, device=None):

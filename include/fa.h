@@ -130,6 +130,16 @@ fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const
  */
 fa_status fa_check_error(fa_stream_t stream);
 
+/*
+ * Failure-detection self test: launches one CTA whose threads wait on a
+ * pipeline barrier that is never signalled, through the same time-bounded
+ * wait every kernel of this library uses.  The wait gives up after limit_ns
+ * nanoseconds (0 < limit_ns <= 1e10) and records FA_ERR_TIMEOUT in the device
+ * error word, so a following fa_check_error(stream) returns FA_ERR_TIMEOUT and
+ * the context stays usable.  Enqueues only; returns FA_OK once launched.
+ */
+fa_status fa_selftest_stalled_wait(uint64_t limit_ns, fa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status status);
 

@@ -32,8 +32,9 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_check_error",
-              "fa_status_string"):
+    for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_main",
+              "fa_bwd_finish", "fa_bwd_workspace_bytes", "fa_check_error", "fa_status_string",
+              "fa_selftest_stalled_wait"):
         assert n in names
 
 
@@ -80,3 +81,19 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.fa_bwd(*args, 1, 1, 128, 64, f(0.125), 0, null, fake, 16, null) == 1
     args[6] = null
     assert lib.fa_bwd(*args, 1, 1, 128, 64, f(0.125), 0, null, fake, 1 << 20, null) == 1
+
+
+def test_selftest_limit_is_validated_on_the_host(lib):
+    null = ctypes.c_void_p(0)
+    assert lib.fa_selftest_stalled_wait(0, null) == 1
+    assert lib.fa_selftest_stalled_wait(20_000_000_000, null) == 1
+
+
+def test_backward_stages_reject_invalid_arguments(lib):
+    fake, null, f = ctypes.c_void_p(0x10000), ctypes.c_void_p(0), ctypes.c_float
+    assert lib.fa_bwd_prepare(null, fake, 1, 1, 128, 64, fake, 1 << 20, null) == 1
+    assert lib.fa_bwd_prepare(fake, fake, 1, 1, 128, 64, fake, 16, null) == 1
+    assert lib.fa_bwd_prepare(fake, fake, 1, 1, 128, 96, fake, 1 << 20, null) == 2
+    assert lib.fa_bwd_main(*([fake] * 7), 1, 1, 128, 64, f(0.1), 0, null, ctypes.c_void_p(0x10010),
+                           1 << 20, null) == 1  # workspace not 256-byte aligned
+    assert lib.fa_bwd_finish(fake, 1, 1, 128, 64, f(0.1), null, 1 << 20, null) == 1
