@@ -331,7 +331,7 @@ def run_ours(args, rank, world):
     threads = cpu_threads()
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        secs, cflops, desc = oracle_sample(2048, threads)
+        secs, cflops, desc = oracle_sample(4096, threads)
         cpu = {"value": cflops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2)}
 
