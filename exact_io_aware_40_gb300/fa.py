@@ -45,6 +45,8 @@ def load_library():
     lib.fa_bwd_prepare.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
     lib.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.fa_bwd_finish.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
+    lib.fa_bwd_noalloc.restype = ctypes.c_int
     lib.fa_selftest_stalled_wait.argtypes = [ctypes.c_uint64, vp]
     lib.fa_check_error.argtypes = [vp]
     lib.fa_status_string.argtypes = [i]
@@ -144,6 +146,16 @@ def fa_bwd_finish(dq, scale, workspace, stream=None):
     B, H, N, d = _shape(dq)
     _check(load_library().fa_bwd_finish(_ptr(dq), B, H, N, d, float(scale), _ptr(workspace),
                                         workspace.numel(), _stream(stream, dq)), "fa_bwd_finish")
+
+
+def fa_bwd_noalloc(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, stream=None):
+    """fa_bwd_noalloc: the backward pass with the library's fixed scratch as the
+    workspace, for callers that cannot allocate device memory (see fa.h)."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
+                                         _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                         int(bool(causal)), _ptr(kv_len), _stream(stream, q)),
+           "fa_bwd_noalloc")
 
 
 def fa_selftest_stalled_wait(limit_ns, stream=None):

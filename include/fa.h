@@ -131,6 +131,39 @@ fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const
 fa_status fa_check_error(fa_stream_t stream);
 
 /*
+ * Capacity of the fixed scratch array behind fa_bwd_noalloc: 64 MiB.  Every GPU
+ * on which the library is loaded holds this much device memory until the
+ * process exits.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fa_bwd without a workspace argument.  The paper and the pages have no
+ * counterpart to this entry point: it exists for callers that cannot allocate
+ * device memory -- code running under a host framework that owns every device
+ * byte through its own pool, and latency-critical paths on which cudaMalloc or
+ * cudaFree could synchronise the device.  It computes exactly what fa_bwd
+ * computes (same kernels, same arguments minus the workspace) and allocates
+ * nothing: its workspace is a file-scope device array of
+ * FA_BWD_NOALLOC_SCRATCH_BYTES bytes inside this library.
+ *   - Size limit: returns FA_ERR_UNSUPPORTED, and enqueues nothing, when
+ *     fa_bwd_workspace_bytes(B, H, N, d) exceeds FA_BWD_NOALLOC_SCRATCH_BYTES
+ *     (for example B=16, H=16, N=512, d=64 fits; B=1, H=16, N=16384, d=128
+ *     does not).
+ *   - First call on a device: looks up the array's device address there
+ *     (cudaGetSymbolAddress, which may load the library's device code on that
+ *     device).  Make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents; each call clears the part that must start at zero.
+ *     Calls whose work overlaps on the GPU (different streams without ordering
+ *     between them) race on the array and give wrong results -- order them.
+ */
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                         fa_stream_t stream);
+
+/*
  * Failure-detection self test: launches one CTA whose threads wait on a
  * pipeline barrier that is never signalled, through the same time-bounded
  * wait every kernel of this library uses.  The wait gives up after limit_ns
