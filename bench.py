@@ -42,11 +42,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 BWD_MAIN_TRAFFIC = {"sha256": None, "bytes_per_launch": None}
 
 
-def pairs(causal, b=B, h=H, n=N):
+def pairs(causal, b=None, h=None, n=None):
+    b, h, n = (B if b is None else b), (H if h is None else h), (N if n is None else n)
     return b * h * (n * (n + 1) // 2 if causal else n * n)
 
 
-def step_flops(b=B, h=H, n=N, d=D):
+def step_flops(b=None, h=None, n=None, d=D):
     return sum(14 * d * pairs(c, b, h, n) for c in (0, 1))
 
 
@@ -371,10 +372,19 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host cores")
+    ap.add_argument("--heads", type=int, default=16,
+                    help="heads of the workload (default 16); fewer heads give the same "
+                         "kernels on a smaller device footprint for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
 
+    global H, WORKLOAD
+    if args.heads != H:
+        if args.heads < 1:
+            ap.error("--heads must be positive")
+        WORKLOAD = WORKLOAD.replace("H=%d" % H, "H=%d" % args.heads)
+        H = args.heads
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
