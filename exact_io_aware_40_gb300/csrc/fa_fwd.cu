@@ -10,16 +10,23 @@
 // the loads of Q, K, V and the store of O and L stays on chip (study notes,
 // section "Kernel融合").
 //
-// GB300 mapping (one CTA per 128-row query block i of one (batch, head)):
-//   warp 0      TMA producer: Q_i once, then K_j and V_j through smem rings
+// GB300 mapping: one CTA owns two 128-row query blocks A and B of one
+// (batch, head) and streams K_j, V_j once for both.
+//   warp 0      TMA producer: Q_A, Q_B once; K_j, V_j through smem rings
 //               (128-byte swizzle, 64-column atoms).
-//   warp 1      tcgen05 issuer (one thread): S_j = Q_i K_j^T into one of two
-//               TMEM S buffers (128 fp32 columns each), O += P_j V_j with P_j
-//               read from TMEM as the A operand.  Also owns TMEM (512 cols).
-//   warps 2-5   softmax: thread t owns query row t (= TMEM lane t); reads its
-//               S row, masks, updates (m, l), writes P (bf16) over the first
-//               64 columns of the same S buffer, rescales O in TMEM when the
-//               row maximum grew, and finally writes O / l (TMA store) and L.
+//   warp 1      tcgen05 issuer (one thread), per key block j:
+//                 O_A += P_A V_j;  S_A = Q_A K_{j+1}^T;  O_B += P_B V_j;  S_B = Q_B K_{j+1}^T
+//               so while one softmax warpgroup works on its S the tensor pipe
+//               runs the other block's products.  Owns TMEM (512 columns:
+//               S_A, S_B at 0 and 128, O_A, O_B at 256 and 256 + d).
+//   warps 4-7   softmax of block A, warps 8-11 softmax of block B: thread t
+//               owns query row t (= TMEM lane t); reads its S row, masks,
+//               updates (m, l), writes P (bf16) over the first 64 columns of
+//               its S buffer, rescales its O row in TMEM when the row maximum
+//               grew by more than 2^8, and finally writes O / l (TMA store) and L.
+// The commit that announces S_X(j+1) also covers every earlier product of the
+// issuing thread, PV_X(j) included, so O_X is stable whenever its softmax
+// warpgroup holds a fresh S_X: the rescale needs no extra wait.
 // Loop order: query block outer (per CTA), key block inner, so O stays in TMEM
 // for the whole loop; the study notes' K/V-outer order computes the same
 // result (they only differ in which operand is reused on chip).
@@ -29,9 +36,11 @@
 namespace fa {
 namespace {
 
-constexpr int kBR = 128;      // query rows per CTA (MMA M)
+constexpr int kBR = 128;      // query rows per block (MMA M)
 constexpr int kBC = 128;      // keys per block (MMA N of S, K of PV)
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kRegsLow = 56;    // warps 0-3 (producer, MMA) after setmaxnreg.dec
+constexpr int kRegsHigh = 224;  // softmax warpgroups after setmaxnreg.inc
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 8
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -42,38 +51,36 @@ struct Cfg {
   static constexpr int kTileBytes = kAtoms * kAtomBytes; // one 128-row bf16 tile
   static constexpr int kKSt = HD == 64 ? 3 : 2;
   static constexpr int kVSt = HD == 64 ? 3 : 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffQ = 0;                          // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKSt * kTileBytes;
   static constexpr int kOffBar = kOffV + kVSt * kTileBytes;
-  // barriers: q_full, k_full[], k_empty[], v_full[], v_empty[], s_full[2],
-  // p_full[2], o_done, drain
-  static constexpr int kNumBar = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 1 + 1;
+  // q_full[2], k_full[], k_empty[], v_full[], v_empty[], s_full[2], p_full[2],
+  // o_final[2], drain
+  static constexpr int kNumBar = 2 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kUsed = kOffMisc + 16;
-  // + 1 KB for aligning the base, + 32 KB of unused tail so that even a
-  // descriptor stride read past the last V stage stays inside the allocation.
-  static constexpr int kSmemBytes = kUsed + 1024 + 32768;
+  static constexpr int kSmemBytes = kUsed + 1024;  // + alignment of the base
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // TMEM columns
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kTmemCols = 512;
 };
 
-__device__ __forceinline__ uint32_t s_col(int b) { return b ? 128u : 0u; }
-
-// Named barrier over 128 threads that also returns the AND of `pred` over them.
-__device__ __forceinline__ bool bar_and_128(int id, bool pred) {
+// Named barrier over `n` threads that also returns the AND of `pred` over them.
+__device__ __forceinline__ bool bar_and(int id, int n, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(id)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
       : "memory");
   return r != 0;
+}
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 template <int HD>
@@ -92,15 +99,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = sb + C::kOffK;
   const uint32_t sV = sb + C::kOffV;
   const uint32_t bar0 = sb + C::kOffBar;
-  const uint32_t bar_q = bar0;
-  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kempty = [&](int s) { return bar0 + 8u * (1 + C::kKSt + s); };
-  auto bar_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * C::kKSt + s); };
-  auto bar_vempty = [&](int s) { return bar0 + 8u * (1 + 2 * C::kKSt + C::kVSt + s); };
-  const uint32_t bar_sfull0 = bar0 + 8u * (1 + 2 * C::kKSt + 2 * C::kVSt);
-  const uint32_t bar_pfull0 = bar_sfull0 + 16u;
-  const uint32_t bar_odone = bar_pfull0 + 16u;
-  const uint32_t bar_drain = bar_odone + 8u;
+  auto bar_qfull = [&](int x) { return bar0 + 8u * x; };
+  auto bar_kfull = [&](int s) { return bar0 + 8u * (2 + s); };
+  auto bar_kempty = [&](int s) { return bar0 + 8u * (2 + C::kKSt + s); };
+  auto bar_vfull = [&](int s) { return bar0 + 8u * (2 + 2 * C::kKSt + s); };
+  auto bar_vempty = [&](int s) { return bar0 + 8u * (2 + 2 * C::kKSt + C::kVSt + s); };
+  const uint32_t bar_s0 = bar0 + 8u * (2 + 2 * C::kKSt + 2 * C::kVSt);
+  auto bar_sfull = [&](int x) { return bar_s0 + 8u * x; };
+  auto bar_pfull = [&](int x) { return bar_s0 + 16u + 8u * x; };
+  auto bar_ofinal = [&](int x) { return bar_s0 + 32u + 8u * x; };
+  const uint32_t bar_drain = bar_s0 + 48u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -108,19 +116,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // Head-major order: the CTAs in flight share one head's K/V (L2 reuse); within
-  // a head the longest query blocks (causal) start first.
-  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
-  const int q0 = qt * kBR;
+  // Head-major order with the longest query blocks (causal) of a head first.
+  const int n_pairs = (a.n_qtiles + 1) / 2;
+  const int bh = static_cast<int>(blockIdx.x / n_pairs);
+  const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs);
+  const int qtA = 2 * pr;
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  int T = (kv_limit + kBC - 1) / kBC;
-  if (a.causal) T = min(T, qt + 1);
+  const int kv_tiles = (kv_limit + kBC - 1) / kBC;
+  const bool hasB = qtA + 1 < a.n_qtiles;
+  // key blocks each query block needs
+  const int TA = a.causal ? min(kv_tiles, qtA + 1) : kv_tiles;
+  const int TB = hasB ? (a.causal ? min(kv_tiles, qtA + 2) : kv_tiles) : 0;
+  const int T = max(TA, TB);
 
   if (tid == 0) {
-    mbar_init(bar_q, 1);
+    mbar_init(bar_qfull(0), 1);
+    mbar_init(bar_qfull(1), 1);
     for (int s = 0; s < C::kKSt; ++s) {
       mbar_init(bar_kfull(s), 1);
       mbar_init(bar_kempty(s), 1);
@@ -129,11 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_vfull(s), 1);
       mbar_init(bar_vempty(s), 1);
     }
-    mbar_init(bar_sfull0, 1);
-    mbar_init(bar_sfull0 + 8, 1);
-    mbar_init(bar_pfull0, 4);
-    mbar_init(bar_pfull0 + 8, 4);
-    mbar_init(bar_odone, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar_sfull(x), 1);
+      mbar_init(bar_pfull(x), 4);
+      mbar_init(bar_ofinal(x), 1);
+    }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -152,14 +165,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && T > 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0 && lane == 0 && T > 0) {
+      // ---------------------------------------------------------- producer
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(bar_q, C::kTileBytes);
-      for (int c = 0; c < C::kAtoms; ++c)
-        tma_load_3d(sQ + c * C::kAtomBytes, &tmQ, c * 64, q0, bh, bar_q, pol_q);
+      for (int x = 0; x < (hasB ? 2 : 1); ++x) {
+        mbar_arrive_expect_tx(bar_qfull(x), C::kTileBytes);
+        for (int c = 0; c < C::kAtoms; ++c)
+          tma_load_3d(sQ + x * C::kTileBytes + c * C::kAtomBytes, &tmQ, c * 64, (qtA + x) * kBR, bh,
+                      bar_qfull(x), pol_q);
+      }
       int last_k[C::kKSt], last_v[C::kVSt];
       for (int s = 0; s < C::kKSt; ++s) last_k[s] = -1;
       for (int s = 0; s < C::kVSt; ++s) last_v[s] = -1;
@@ -182,78 +199,100 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Unwinding: let the copies already issued land before the CTA exits.
         // Load j is the (j / stages)-th use of its stage, so its completion is
         // the phase of that parity.
-        mbar_wait_drain(bar_q, 0);
+        mbar_wait_drain(bar_qfull(0), 0);
+        if (hasB) mbar_wait_drain(bar_qfull(1), 0);
         for (int s = 0; s < C::kKSt; ++s)
           if (last_k[s] >= 0) mbar_wait_drain(bar_kfull(s), (last_k[s] / C::kKSt) & 1);
         for (int s = 0; s < C::kVSt; ++s)
           if (last_v[s] >= 0) mbar_wait_drain(bar_vfull(s), (last_v[s] / C::kVSt) & 1);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && T > 0) {
+    } else if (warp == 1 && lane == 0 && T > 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idS = idesc_bf16(kBR, kBC, false, false);
       constexpr uint32_t idO = idesc_bf16(kBR, HD, false, true);
-      bool ok = mbar_wait(bar_q, 0, ab);
-      auto issue_pv = [&](int jj) -> bool {
-        const int bb = jj & 1, vs = jj % C::kVSt;
-        if (!mbar_wait(bar_pfull0 + 8u * bb, (jj >> 1) & 1, ab)) return false;
-        if (!mbar_wait(bar_vfull(vs), (jj / C::kVSt) & 1, ab)) return false;
+      bool ok = true;
+      // S_X(j) = Q_X K_j^T into S buffer X (columns 128 X).
+      auto issue_s = [&](int x, int j) -> bool {
+        const int ks = j % C::kKSt;
+        if (j == 0 && !mbar_wait(bar_qfull(x), 0, ab)) return false;
+        if (!mbar_wait(bar_kfull(ks), (j / C::kKSt) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t vbase = sV + vs * C::kTileBytes;
-#pragma unroll
-        for (int k = 0; k < kBC / 16; ++k) {
-          // B = V_j, MN-major: 16 key rows per step (two 8-row groups, SBO
-          // 1024 B); 64-column atoms of d are kAtomBytes apart (LBO).
-          const uint64_t bdesc = sdesc_sw128(vbase + k * 2048, C::kAtomBytes, 1024);
-          mma_ts(tmem + C::kColO, tmem + s_col(bb) + k * 8, bdesc, idO, (jj > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(bar_odone);
-        mma_commit(bar_vempty(vs));
-        return true;
-      };
-      for (int j = 0; ok && j < T; ++j) {
-        const int bb = j & 1, ks = j % C::kKSt;
-        if (j >= 2 && !mbar_wait(bar_odone, (j - 2) & 1, ab)) { ok = false; break; }
-        if (!mbar_wait(bar_kfull(ks), (j / C::kKSt) & 1, ab)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kbase = sK + ks * C::kTileBytes;
+        const uint32_t qbase = sQ + x * C::kTileBytes, kbase = sK + ks * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           // K-major operands: step k covers columns [16k, 16k+16) of d, i.e.
           // atom k/4, byte offset 32*(k%4) inside the 128-byte swizzled row.
           const uint32_t off = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
-          mma_ss(tmem + s_col(bb), sdesc_sw128(sQ + off, 16, 1024),
+          mma_ss(tmem + 128u * x, sdesc_sw128(qbase + off, 16, 1024),
                  sdesc_sw128(kbase + off, 16, 1024), idS, k > 0 ? 1u : 0u);
         }
-        mma_commit(bar_sfull0 + 8u * bb);
-        mma_commit(bar_kempty(ks));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(bar_sfull(x));
+        // the last reader of K_j releases its stage
+        if (x == 1 || j >= TB) mma_commit(bar_kempty(ks));
+        return true;
+      };
+      // O_X (+)= P_X(j) V_j with P_X read from TMEM.
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int vs = j % C::kVSt;
+        if (!mbar_wait(bar_pfull(x), j & 1, ab)) return false;
+        // the first reader of V_j waits for it
+        if ((x == 0 || j >= TA) && !mbar_wait(bar_vfull(vs), (j / C::kVSt) & 1, ab)) return false;
+        tc_fence_after();
+        const uint32_t vbase = sV + vs * C::kTileBytes;
+        const uint32_t ocol = C::kColO + static_cast<uint32_t>(HD) * x;
+#pragma unroll
+        for (int k = 0; k < kBC / 16; ++k) {
+          // B = V_j, MN-major: 16 key rows per step (two 8-row groups, SBO
+          // 1024 B); 64-column atoms of d are kAtomBytes apart (LBO).
+          const uint64_t bdesc = sdesc_sw128(vbase + k * 2048, C::kAtomBytes, 1024);
+          mma_ts(tmem + ocol, tmem + 128u * x + k * 8, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        if (j == (x == 0 ? TA : TB) - 1) mma_commit(bar_ofinal(x));
+        if (x == 1 || j >= TB) mma_commit(bar_vempty(vs));
+        return true;
+      };
+      if (TA > 0) ok = issue_s(0, 0);
+      if (ok && TB > 0) ok = issue_s(1, 0);
+      for (int j = 0; ok && j < T; ++j) {
+        // S_X(j+1) overwrites P_X(j): the product just before it reads P_X(j)
+        // first (MMAs of one thread execute in issue order).
+        if (j < TA) {
+          ok = issue_pv(0, j);
+          if (ok && j + 1 < TA) ok = issue_s(0, j + 1);
+        }
+        if (ok && j < TB) {
+          ok = issue_pv(1, j);
+          if (ok && j + 1 < TB) ok = issue_s(1, j + 1);
+        }
       }
-      if (ok) issue_pv(T - 1);
       // Drain: all MMAs issued above complete before TMEM is released.
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0);
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ------------------------------------------------------------ softmax
+    const int x = (warp >> 2) - 1;          // 0: block A (warps 4-7), 1: block B (warps 8-11)
+    const int Tn = x == 0 ? TA : TB;        // TB = 0 when there is no block B
     const int quarter = warp & 3;           // TMEM lanes [32*quarter, +32)
     const int row = quarter * 32 + lane;    // row of the tile = TMEM lane
+    const int q0 = (qtA + x) * kBR;
     const int grow = q0 + row;              // query index
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t scol = 128u * x;
+    const uint32_t ocol = C::kColO + static_cast<uint32_t>(HD) * x;
     float m_run = -INFINITY;                // running max, log2 units (scaled)
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int bb = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull0 + 8u * bb, (j >> 1) & 1, ab))) {
+    for (int j = 0; j < Tn; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(x), j & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + s_col(bb) + 32 * c, sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + 32 * c, sr[c]);
       tmem_wait_ld();
       const int key0 = j * kBC;
       const bool need_mask = (key0 + kBC > kv_limit) || (a.causal && key0 + kBC - 1 > q0);
@@ -293,57 +332,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e] = pack_bf16(p0, p1);
         }
         // P occupies the first 64 columns of the S buffer (2 bf16 per column).
-        tmem_st16(tl + s_col(bb) + 16 * c, pk);
+        tmem_st16(tl + scol + 16 * c, pk);
       }
       l_run = l_run * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
       m_run = m_new;
       if (j > 0 && __any_sync(0xffffffffu, grow_max)) {
-        // O holds P_0..P_{j-1} V; rescale it once PV_{j-1} has landed.  (Only
-        // PV_{j-1} can be pending: PV_{j-2} completed before S_j was issued, so
-        // the parity of this wait is unambiguous even when earlier ones were
-        // skipped.)
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, ab))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        {
+        // O_X holds P_X(0..j-1) V; every product writing it has completed (see
+        // the header), so it can be rescaled in place.
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tl + C::kColO + 32 * c, o);
-            tmem_wait_ld();
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + ocol + 32 * c, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tl + C::kColO + 32 * c, o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tl + ocol + 32 * c, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull0 + 8u * bb);
+      if (lane == 0) mbar_arrive(bar_pfull(x));
     }
-    if (ok && T > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_odone, (T - 1) & 1, ab));
+    if (ok && Tn > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_ofinal(x), 0, ab));
       tc_fence_after();
     }
-    // All four softmax warps take the same branch: AND of every thread's ok.
-    ok = bar_and_128(1, ok && *abort_flag == 0);
-    if (ok) {
+    // All four warps of this warpgroup take the same branch.
+    ok = bar_and(1 + x, 128, ok && *abort_flag == 0);
+    if (ok && (x == 0 || hasB)) {
       // ---------------------------------------------------------- epilogue
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       if (grow < a.N) {
         const float Lv = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         a.L[static_cast<long long>(bh) * a.N + grow] = Lv;
       }
-      // O / l -> bf16 -> the (now idle) Q tile buffer, in the same swizzled
-      // layout TMA uses, then one TMA store per 64-column atom.
+      // O / l -> bf16 -> the (now idle) Q_X tile buffer, in the same swizzled
+      // layout TMA uses, then one TMA store per 64-column atom.  Every lane
+      // takes part in the warp-collective TMEM loads; TMA clips rows >= N.
+      const int qoff = C::kOffQ + x * C::kTileBytes;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
-        if (T > 0) {
-          tmem_ld32(tl + C::kColO + 32 * c, o);
+        if (Tn > 0) {
+          tmem_ld32(tl + ocol + 32 * c, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -359,13 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           v.z = pack_bf16(__uint_as_float(o[8 * t + 4]) * inv_l, __uint_as_float(o[8 * t + 5]) * inv_l);
           v.w = pack_bf16(__uint_as_float(o[8 * t + 6]) * inv_l, __uint_as_float(o[8 * t + 7]) * inv_l);
           const int phys = (chunk0 + t) ^ (row & 7);
-          *reinterpret_cast<uint4*>(smem + C::kOffQ + atom * C::kAtomBytes + row * 128 + phys * 16) = v;
+          *reinterpret_cast<uint4*>(smem + qoff + atom * C::kAtomBytes + row * 128 + phys * 16) = v;
         }
       }
       fence_proxy_async_smem();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (warp == 2 && lane == 0) {
-        for (int c = 0; c < C::kAtoms; ++c) tma_store_3d(&tmO, sQ + c * C::kAtomBytes, c * 64, q0, bh);
+      bar_sync(1 + x, 128);
+      if (quarter == 0 && lane == 0) {
+        for (int c = 0; c < C::kAtoms; ++c)
+          tma_store_3d(&tmO, sQ + x * C::kTileBytes + c * C::kAtomBytes, c * 64, q0, bh);
         bulk_commit();
         bulk_wait0();
       }
@@ -389,12 +422,18 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
+    // The register split (setmaxnreg) must fit in what the launch provides,
+    // or the increasing warpgroups would wait for registers forever.
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, fa_fwd_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    if (fattr.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh) return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(fa_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
+  const long long grid = static_cast<long long>((a.n_qtiles + 1) / 2) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fa_fwd_kernel<HD><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,

@@ -69,7 +69,9 @@ constexpr uint32_t kMaxWaitRounds = 1u << 20;
 // Waits for the phase with the given parity to complete.  Gives up (and
 // returns false) when the time limit passes, when another role of this CTA
 // gave up, or when another CTA recorded an error.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a,
+// (Inlined: a kernel whose warpgroups run under different setmaxnreg budgets
+// cannot share one out-of-line copy between them.)
+static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a,
                                               uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -90,7 +92,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abo
 }
 
 // Same, without an abort context: only for drain waits during unwinding.
-static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+static __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   for (uint32_t round = 0; !mbar_try_wait(bar, parity); ++round)
     if (globaltimer() - t0 > kWaitLimitNs || round >= 32u * kMaxWaitRounds) return false;
