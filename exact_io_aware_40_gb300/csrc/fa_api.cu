@@ -81,6 +81,22 @@ fa_status map_bf16(EncodeTiledFn enc, CUtensorMap* m, const void* base, int d,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// Tensor map over the fp32 [BH, N, d] dQ accumulator, no swizzle, box
+// (d, rows, 1): the target of the backward kernel's bulk reduce-adds.
+fa_status map_f32_acc(EncodeTiledFn enc, CUtensorMap* m, const void* base, int d, int N, int BH,
+                      int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(N)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_common(int B, int H, int N, int d, float scale) {
@@ -240,10 +256,13 @@ fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* d
   float *dq_acc, *Dvec;
   workspace_parts(workspace, BH, N, d, &dq_acc, &Dvec);
   CUtensorMap tq, tk, tv, tdo;
-  if ((st = map_bf16(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
+  const int qrows = fa::bwd_query_rows(d);
+  if ((st = map_bf16(enc, &tq, Q, d, N, BH, qrows)) != FA_OK) return st;
   if ((st = map_bf16(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
   if ((st = map_bf16(enc, &tv, V, d, N, BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tdo, dO, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tdo, dO, d, N, BH, qrows)) != FA_OK) return st;
+  CUtensorMap tdq;
+  if ((st = map_f32_acc(enc, &tdq, dq_acc, d, N, BH, qrows)) != FA_OK) return st;
   fa::BwdArgs a;
   a.L = L;
   a.D = Dvec;
@@ -256,11 +275,11 @@ fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* d
   a.N = N;
   a.BH = BH;
   a.n_ktiles = (N + 127) / 128;
-  a.n_qtiles = (N + 127) / 128;
+  a.n_qtiles = (N + qrows - 1) / qrows;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
-  return fa::launch_bwd(d, tq, tk, tv, tdo, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return fa::launch_bwd(d, tq, tk, tv, tdo, tdq, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,

@@ -46,9 +46,14 @@ struct BwdArgs {
   float scale_log2;     // scale * log2(e)
   int causal;
 };
+// Rows per query tile of the backward kernel's TMA boxes for Q and dO.
+inline int bwd_query_rows(int d) { return d == 128 ? 64 : 128; }
+
+// tmdQ: fp32 view of the dQ accumulator (box: d columns x 64 rows), used by
+// the d = 128 kernel's bulk reductions.
 cudaError_t launch_bwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdArgs& a,
-                       cudaStream_t stream);
+                       const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
+                       const BwdArgs& a, cudaStream_t stream);
 
 struct BwdPostArgs {
   const float* dq_acc;  // fp32 [BH, N, d]
