@@ -4,11 +4,12 @@
 One step = the whole hot path over one batch of the long-sequence workload
 (B=1, H=16, N=16384, d=128, bf16, iid N(0,1) inputs from the seeded
 generator): for causal = 0 and 1, the forward pass (fa_fwd) and the three
-backward stages (fa_bwd_prepare, fa_bwd_main, fa_bwd_finish).
+backward stages (fa_bwd_prepare, fa_bwd_dkdv, fa_bwd_dq).
 
 FLOPs are counted over the unmasked (query, key) pairs P of each pass:
 forward 4*d*P (QK^T and PV), backward 10*d*P (QK^T recomputed, dP, dV, dK,
-dQ); non-causal P = B*H*N^2, causal P = B*H*N(N+1)/2.
+dQ); non-causal P = B*H*N^2, causal P = B*H*N(N+1)/2.  The dQ kernel recomputes
+QK^T and dP a second time; those 4*d*P are not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -36,10 +37,10 @@ SEED = 1003  # the long-sequence workload's seed
 WORKLOAD = "long-sequence attention B=1 H=16 N=16384 d=128 bf16, fwd+bwd, causal=0 and causal=1"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
-# DRAM traffic of one fa_bwd_main launch on this workload (dram__bytes_read.sum +
+# DRAM traffic of one fa_bwd_dkdv launch on this workload (dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
 # launches), valid only while the kernel source hashes to the recorded digest.
-BWD_MAIN_TRAFFIC = {"sha256": None, "bytes_per_launch": None}
+BWD_DKDV_TRAFFIC = {"sha256": None, "bytes_per_launch": None}
 
 
 def pairs(causal, b=None, h=None, n=None):
@@ -216,7 +217,7 @@ def run_ours(args, rank, world):
     ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    stages = ("fwd", "prep", "main", "finish")
+    stages = ("fwd", "prep", "dkdv", "dq")
 
     def step(ev=None):
         for c in (0, 1):
@@ -229,10 +230,10 @@ def run_ours(args, rank, world):
             fa.fa_bwd_prepare(t["o"], do, ws, stream=sp)
             if ev is not None:
                 ev[c][2].record(stream)
-            fa.fa_bwd_main(q, k, v, do, t["L"], t["dk"], t["dv"], scale, c, None, ws, stream=sp)
+            fa.fa_bwd_dkdv(q, k, v, do, t["L"], t["dk"], t["dv"], scale, c, None, ws, stream=sp)
             if ev is not None:
                 ev[c][3].record(stream)
-            fa.fa_bwd_finish(t["dq"], scale, ws, stream=sp)
+            fa.fa_bwd_dq(q, k, v, do, t["L"], t["dq"], scale, c, None, ws, stream=sp)
             if ev is not None:
                 ev[c][4].record(stream)
 
@@ -318,16 +319,20 @@ def run_ours(args, rank, world):
         return
 
     peaks, peak_src = load_peaks()
-    main_ms = sum(per_stage[c]["main"] for c in (0, 1)) / (2 * args.steps)
-    main_flops = sum(10 * D * pairs(c) for c in (0, 1)) / 2
-    achieved = main_flops / (main_ms * 1e-3) / 1e12
+    # the longest kernel of the step, with its own algorithmic FLOPs per launch:
+    # fa_bwd_dkdv computes QK^T, dP, dV, dK (8 d P); fa_bwd_dq adds dQ (2 d P)
+    # on top of recomputing QK^T and dP, which are already counted.
+    dkdv_ms = sum(per_stage[c]["dkdv"] for c in (0, 1)) / (2 * args.steps)
+    dq_ms = sum(per_stage[c]["dq"] for c in (0, 1)) / (2 * args.steps)
+    dkdv_flops = sum(8 * D * pairs(c) for c in (0, 1)) / 2
+    achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     traffic = None
-    if BWD_MAIN_TRAFFIC["sha256"] == kernel_digest():
-        traffic = BWD_MAIN_TRAFFIC["bytes_per_launch"]
+    if BWD_DKDV_TRAFFIC["sha256"] == kernel_digest():
+        traffic = BWD_DKDV_TRAFFIC["bytes_per_launch"]
     fwd_ms = sum(per_stage[c]["fwd"] for c in (0, 1)) / args.steps
-    bwd_ms = sum(per_stage[c][st] for c in (0, 1) for st in ("prep", "main", "finish")) / args.steps
+    bwd_ms = sum(per_stage[c][st] for c in (0, 1) for st in ("prep", "dkdv", "dq")) / args.steps
 
     threads = cpu_threads()
     cpu = None
@@ -344,7 +349,7 @@ def run_ours(args, rank, world):
                    "passes": "fwd+bwd", "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (Q, K, V, dO, outputs: 64 MiB each; 128 MiB fp32 "
                          "dQ accumulator) -- no flush between steps"},
-        "roofline": {"bound": "tensor", "kernel": "fa_bwd_main (mean of causal 0/1 launches)",
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd_dkdv (mean of causal 0/1 launches)",
                      "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                      "traffic": traffic,
                      "peak_source": "bf16_tflops_sustained of %s peaks" % peak_src,
@@ -359,6 +364,8 @@ def run_ours(args, rank, world):
             "bwd_ms": bwd_ms,
             "bwd_tflops": sum(10 * D * pairs(c) for c in (0, 1)) / (bwd_ms * 1e-3) / 1e12,
             "stage_ms": {str(c): {st: per_stage[c][st] / args.steps for st in stages} for c in (0, 1)},
+            "dq_kernel_tflops": {"algorithmic": sum(2 * D * pairs(c) for c in (0, 1)) / 2 / (dq_ms * 1e-3) / 1e12,
+                                 "executed": sum(6 * D * pairs(c) for c in (0, 1)) / 2 / (dq_ms * 1e-3) / 1e12},
         },
     }
     print(json.dumps(line), flush=True)

@@ -81,22 +81,6 @@ fa_status map_bf16(EncodeTiledFn enc, CUtensorMap* m, const void* base, int d,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// Tensor map over the fp32 [BH, N, d] dQ accumulator, no swizzle, box
-// (d, rows, 1): the target of the backward kernel's bulk reduce-adds.
-fa_status map_f32_acc(EncodeTiledFn enc, CUtensorMap* m, const void* base, int d, int N, int BH,
-                      int rows) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
-                           static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(N)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_common(int B, int H, int N, int d, float scale) {
@@ -199,15 +183,7 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
-}
-
-// Splits the workspace into the fp32 dQ accumulator and the fp32 D vector.
-static void workspace_parts(void* ws, int BH, int N, int d, float** dq_acc, float** Dvec) {
-  const size_t rows = static_cast<size_t>(BH) * N;
-  *dq_acc = static_cast<float*>(ws);
-  *Dvec = reinterpret_cast<float*>(static_cast<char*>(ws) + round256(rows * d * sizeof(float)));
+  return round256(static_cast<size_t>(B) * H * N * sizeof(float));
 }
 
 static fa_status check_workspace(const void* ws, size_t bytes, int B, int H, int N, int d) {
@@ -223,80 +199,89 @@ fa_status fa_bwd_prepare(const void* O, const void* dO, int B, int H, int N, int
   if (st != FA_OK) return st;
   if (!aligned(O, 16) || !aligned(dO, 16)) return FA_ERR_INVALID_ARG;
   if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
-  float *dq_acc, *Dvec;
-  workspace_parts(workspace, B * H, N, d, &dq_acc, &Dvec);
   fa::BwdPreArgs pre;
   pre.O = static_cast<const uint16_t*>(O);
   pre.dO = static_cast<const uint16_t*>(dO);
-  pre.D = Dvec;
-  pre.dq_acc = dq_acc;
+  pre.D = static_cast<float*>(workspace);
   pre.rows = static_cast<long long>(B) * H * N;
   pre.d = d;
   return fa::launch_bwd_pre(pre, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
-                      const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
-                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
-                      fa_stream_t stream) {
-  if (!Q || !K || !V || !dO || !L || !dK || !dV) return FA_ERR_INVALID_ARG;
+// Shared validation and argument block of the two recompute kernels.
+static fa_status bwd_args(const void* Q, const void* K, const void* V, const void* dO,
+                          const float* L, int B, int H, int N, int d, float scale, int causal,
+                          const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
+                          fa::BwdArgs* a, EncodeTiledFn* enc) {
+  if (!Q || !K || !V || !dO || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) ||
-      !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
+      !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
   if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
   int dev;
   if ((st = current_device(&dev)) != FA_OK) return st;
   int* err;
   if ((st = error_word(dev, &err)) != FA_OK) return st;
-  EncodeTiledFn enc;
-  if ((st = encoder(&enc)) != FA_OK) return st;
-  const int BH = B * H;
-  float *dq_acc, *Dvec;
-  workspace_parts(workspace, BH, N, d, &dq_acc, &Dvec);
-  CUtensorMap tq, tk, tv, tdo;
-  const int qrows = fa::bwd_query_rows(d);
-  if ((st = map_bf16(enc, &tq, Q, d, N, BH, qrows)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tv, V, d, N, BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tdo, dO, d, N, BH, qrows)) != FA_OK) return st;
-  CUtensorMap tdq;
-  if ((st = map_f32_acc(enc, &tdq, dq_acc, d, N, BH, qrows)) != FA_OK) return st;
-  fa::BwdArgs a;
-  a.L = L;
-  a.D = Dvec;
-  a.dq_acc = dq_acc;
-  a.dK = static_cast<uint16_t*>(dK);
-  a.dV = static_cast<uint16_t*>(dV);
-  a.kv_len = kv_len;
-  a.err = err;
-  a.H = H;
-  a.N = N;
-  a.BH = BH;
-  a.n_ktiles = (N + 127) / 128;
-  a.n_qtiles = (N + qrows - 1) / qrows;
-  a.scale = scale;
-  a.scale_log2 = scale * kLog2e;
-  a.causal = causal ? 1 : 0;
-  return fa::launch_bwd(d, tq, tk, tv, tdo, tdq, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if ((st = encoder(enc)) != FA_OK) return st;
+  a->L = L;
+  a->D = static_cast<const float*>(workspace);
+  a->dK = nullptr;
+  a->dV = nullptr;
+  a->kv_len = kv_len;
+  a->err = err;
+  a->H = H;
+  a->N = N;
+  a->BH = B * H;
+  a->n_ktiles = (N + 127) / 128;
+  a->n_qtiles = 0;
+  a->scale = scale;
+  a->scale_log2 = scale * kLog2e;
+  a->causal = causal ? 1 : 0;
+  return FA_OK;
 }
 
-fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
-                        size_t workspace_bytes, fa_stream_t stream) {
-  if (!dQ) return FA_ERR_INVALID_ARG;
-  fa_status st = check_common(B, H, N, d, scale);
+fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO,
+                      const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                      int causal, const int32_t* kv_len, const void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream) {
+  if (!dK || !dV || !aligned(dK, 16) || !aligned(dV, 16)) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a;
+  EncodeTiledFn enc;
+  fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, workspace,
+                          workspace_bytes, &a, &enc);
   if (st != FA_OK) return st;
-  if (!aligned(dQ, 16)) return FA_ERR_INVALID_ARG;
-  if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
-  float *dq_acc, *Dvec;
-  workspace_parts(const_cast<void*>(workspace), B * H, N, d, &dq_acc, &Dvec);
-  fa::BwdPostArgs post;
-  post.dq_acc = dq_acc;
-  post.dQ = static_cast<uint16_t*>(dQ);
-  post.n = static_cast<long long>(B) * H * N * d;
-  post.scale = scale;
-  return fa::launch_bwd_post(post, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  a.dK = static_cast<uint16_t*>(dK);
+  a.dV = static_cast<uint16_t*>(dV);
+  a.n_qtiles = (N + 63) / 64;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = map_bf16(enc, &tq, Q, d, N, a.BH, 64)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, a.BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, a.BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tdo, dO, d, N, a.BH, 64)) != FA_OK) return st;
+  return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, const float* L,
+                    void* dQ, int B, int H, int N, int d, float scale, int causal,
+                    const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+  if (!dQ || !aligned(dQ, 16)) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a;
+  EncodeTiledFn enc;
+  fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, workspace,
+                          workspace_bytes, &a, &enc);
+  if (st != FA_OK) return st;
+  a.n_qtiles = (N + 127) / 128;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if ((st = map_bf16(enc, &tq, Q, d, N, a.BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, a.BH, 64)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, a.BH, 64)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tdo, dO, d, N, a.BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tdq, dQ, d, N, a.BH, 128)) != FA_OK) return st;
+  return fa::launch_bwd_dq(d, tq, tk, tv, tdo, tdq, a, stream) == cudaSuccess ? FA_OK
+                                                                              : FA_ERR_CUDA;
 }
 
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
@@ -314,10 +299,11 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
   if ((st = fa_bwd_prepare(O, dO, B, H, N, d, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
-  if ((st = fa_bwd_main(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, workspace,
+  if ((st = fa_bwd_dkdv(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, workspace,
                         workspace_bytes, stream)) != FA_OK)
     return st;
-  return fa_bwd_finish(dQ, B, H, N, d, scale, workspace, workspace_bytes, stream);
+  return fa_bwd_dq(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, workspace,
+                   workspace_bytes, stream);
 }
 
 fa_status fa_check_error(fa_stream_t stream) {

@@ -1,13 +1,13 @@
 // fa_bwd_noalloc.cu -- the backward pass for callers that cannot allocate
 // device memory.
 //
-// fa_bwd needs a caller-provided workspace (the fp32 dQ accumulator and the
-// fp32 row terms D).  Some callers cannot produce one: code that runs under a
+// fa_bwd needs a caller-provided workspace (the fp32 row terms D of the
+// softmax gradient).  Some callers cannot produce one: code that runs under a
 // host framework that owns every device byte through its own pool and forbids
 // allocating behind its back, and latency-critical paths where cudaMalloc or
 // cudaFree may synchronise the whole device.  fa_bwd_noalloc serves them from
 // a fixed scratch array compiled into this library instead.  It runs exactly
-// the kernels of fa_bwd (prepare, main, finish), with the scratch array as the
+// the kernels of fa_bwd (prepare, dK/dV, dQ), with the scratch array as the
 // workspace; it calls no allocator.
 #include <cuda_runtime.h>
 
@@ -60,8 +60,9 @@ extern "C" fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V,
   void* scratch = nullptr;
   fa_status st = scratch_address(&scratch);
   if (st != FA_OK) return st;
-  // fa_bwd validates the remaining arguments; its prepare stage zeroes the
-  // accumulator part of the scratch, so no state of an earlier call leaks in.
+  // fa_bwd validates the remaining arguments; its prepare stage overwrites the
+  // scratch before the other stages read it, so no state of an earlier call
+  // leaks in.
   return fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, scratch, need,
                 stream);
 }

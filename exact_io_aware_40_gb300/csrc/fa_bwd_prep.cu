@@ -1,10 +1,7 @@
-// fa_bwd_prepost.cu -- the two HBM-bound helper passes around the backward
-// kernel.
-//
-//   pre : D_i = sum_c dO_ic * O_ic (fp32) for every row, and zero the fp32 dQ
-//         accumulator.  D_i equals sum_j P_ij dP_ij, the row term of the
-//         softmax gradient dS = P o (dP - D), because O_i = sum_j P_ij V_j.
-//   post: dQ = bf16(scale * dQ_acc), round to nearest even.
+// fa_bwd_prep.cu -- the HBM-bound pass before the backward kernels:
+// D_i = sum_c dO_ic * O_ic (fp32) for every row.  D_i equals sum_j P_ij dP_ij,
+// the row term of the softmax gradient dS = P o (dP - D), because
+// O_i = sum_j P_ij V_j.
 #include "kernels.h"
 
 namespace fa {
@@ -28,33 +25,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPreArgs a) {
     acc = bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
           bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
           bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
-    float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   for (int w = tpr / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
   if (row < a.rows && part == 0) a.D[row] = acc;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__global__ void __launch_bounds__(256) bwd_post_kernel(BwdPostArgs a) {
-  const long long n8 = a.n / 8;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 x = reinterpret_cast<const float4*>(a.dq_acc)[2 * i];
-    const float4 y = reinterpret_cast<const float4*>(a.dq_acc)[2 * i + 1];
-    uint4 o;
-    o.x = pack2(x.x * a.scale, x.y * a.scale);
-    o.y = pack2(x.z * a.scale, x.w * a.scale);
-    o.z = pack2(y.x * a.scale, y.y * a.scale);
-    o.w = pack2(y.z * a.scale, y.w * a.scale);
-    reinterpret_cast<uint4*>(a.dQ)[i] = o;
-  }
 }
 
 }  // namespace
@@ -66,15 +39,6 @@ cudaError_t launch_bwd_pre(const BwdPreArgs& a, cudaStream_t stream) {
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_post(const BwdPostArgs& a, cudaStream_t stream) {
-  const long long n8 = a.n / 8;
-  if (n8 <= 0) return cudaSuccess;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;  // grid-stride: 16 blocks per SM
-  bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

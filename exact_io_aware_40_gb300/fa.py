@@ -43,16 +43,16 @@ def load_library():
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.fa_bwd_prepare.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
-    lib.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
-    lib.fa_bwd_finish.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
     lib.fa_bwd_noalloc.restype = ctypes.c_int
     lib.fa_selftest_stalled_wait.argtypes = [ctypes.c_uint64, vp]
     lib.fa_check_error.argtypes = [vp]
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
-    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_main",
-               "fa_bwd_finish", "fa_check_error", "fa_selftest_stalled_wait"):
+    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_dkdv",
+               "fa_bwd_dq", "fa_check_error", "fa_selftest_stalled_wait"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -126,26 +126,28 @@ def fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stre
 
 
 def fa_bwd_prepare(o, do, workspace, stream=None):
-    """fa_bwd_prepare: D = rowsum(dO * O) and a zeroed dQ accumulator in workspace."""
+    """fa_bwd_prepare: D = rowsum(dO * O) into the workspace."""
     B, H, N, d = _shape(o)
     _check(load_library().fa_bwd_prepare(_ptr(o), _ptr(do), B, H, N, d, _ptr(workspace),
                                          workspace.numel(), _stream(stream, o)), "fa_bwd_prepare")
 
 
-def fa_bwd_main(q, k, v, do, L, dk, dv, scale, causal, kv_len, workspace, stream=None):
-    """fa_bwd_main: dK, dV, and dS K added into the workspace's dQ accumulator."""
+def fa_bwd_dkdv(q, k, v, do, L, dk, dv, scale, causal, kv_len, workspace, stream=None):
+    """fa_bwd_dkdv: dK and dV from a prepared workspace."""
     B, H, N, d = _shape(q)
-    _check(load_library().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(dk),
+    _check(load_library().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(dk),
                                       _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                                       _ptr(kv_len), _ptr(workspace), workspace.numel(),
-                                      _stream(stream, q)), "fa_bwd_main")
+                                      _stream(stream, q)), "fa_bwd_dkdv")
 
 
-def fa_bwd_finish(dq, scale, workspace, stream=None):
-    """fa_bwd_finish: dQ = bf16(scale * accumulator)."""
-    B, H, N, d = _shape(dq)
-    _check(load_library().fa_bwd_finish(_ptr(dq), B, H, N, d, float(scale), _ptr(workspace),
-                                        workspace.numel(), _stream(stream, dq)), "fa_bwd_finish")
+def fa_bwd_dq(q, k, v, do, L, dq, scale, causal, kv_len, workspace, stream=None):
+    """fa_bwd_dq: dQ from a prepared workspace."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(dq),
+                                    B, H, N, d, float(scale), int(bool(causal)), _ptr(kv_len),
+                                    _ptr(workspace), workspace.numel(), _stream(stream, q)),
+           "fa_bwd_dq")
 
 
 def fa_bwd_noalloc(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, stream=None):

@@ -81,9 +81,9 @@ fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, flo
                        fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: an fp32 [B, H, N, d] accumulator for
- * dQ plus the fp32 [B, H, N] row terms D_i = sum_c dO_ic O_ic, each region
- * rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_bwd needs: the fp32 [B, H, N] row terms
+ * D_i = sum_c dO_ic O_ic, rounded up to 256 bytes.  Returns 0 for invalid
+ * sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -94,7 +94,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dK = scale dS^T Q,  with D_i = sum_c dO_ic O_ic.
  *   Q, K, V, O, dO  in : bf16 [B, H, N, d]   (O and L from fa_fwd/fa_fwd_kvlen
  *   L               in : fp32 [B, H, N]       with the same scale/mask)
- *   dQ, dK, dV     out : bf16 [B, H, N, d]
+ *   dQ, dK, dV     out : bf16 [B, H, N, d]; all three are deterministic
+ *                        (no atomics: the same inputs give the same bits)
  *   workspace          : device, >= fa_bwd_workspace_bytes(B,H,N,d) bytes,
  *                        256-byte aligned; contents on entry are ignored.
  * Gradients with respect to L are not part of this interface.
@@ -107,35 +108,30 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 /*
  * The three stages fa_bwd enqueues, for callers that want to schedule or time
  * them separately.  Arguments mean the same as in fa_bwd; each validates its
- * own arguments.  fa_bwd == fa_bwd_prepare; fa_bwd_main; fa_bwd_finish.
- *   fa_bwd_prepare: D_i = sum_c dO_ic O_ic into the workspace and zeroes the
- *                   workspace's fp32 dQ accumulator (HBM-bound).
- *   fa_bwd_main:    the recompute kernel: writes dK, dV and adds dS K into the
- *                   workspace's dQ accumulator.  Needs a prepared workspace.
- *   fa_bwd_finish:  dQ = bf16(scale * accumulator) (HBM-bound).
+ * own arguments.  fa_bwd == fa_bwd_prepare; fa_bwd_dkdv; fa_bwd_dq.
+ *   fa_bwd_prepare: D_i = sum_c dO_ic O_ic into the workspace (HBM-bound).
+ *   fa_bwd_dkdv:    one pass per 128-key block over all query rows: dK, dV.
+ *                   Needs a prepared workspace.
+ *   fa_bwd_dq:      one pass per 128-row query block over all keys: dQ.
+ *                   Needs a prepared workspace; independent of fa_bwd_dkdv.
  */
 fa_status fa_bwd_prepare(const void* O, const void* dO, int B, int H, int N, int d,
                          void* workspace, size_t workspace_bytes, fa_stream_t stream);
-fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO,
                       const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
-                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
-                      fa_stream_t stream);
-fa_status fa_bwd_finish(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
-                        size_t workspace_bytes, fa_stream_t stream);
+                      int causal, const int32_t* kv_len, const void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream);
+fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, const float* L,
+                    void* dQ, int B, int H, int N, int d, float scale, int causal,
+                    const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
 
 /*
- * Synchronises `stream`, then returns and clears the current device's error
- * word (FA_ERR_TIMEOUT if a kernel gave up), or FA_ERR_CUDA if the stream
- * itself reports an error.
- */
-fa_status fa_check_error(fa_stream_t stream);
-
-/*
- * Capacity of the fixed scratch array behind fa_bwd_noalloc: 64 MiB.  Every GPU
- * on which the library is loaded holds this much device memory until the
+ * Capacity of the fixed scratch array behind fa_bwd_noalloc: 16 MiB.  Every
+ * GPU on which the library is loaded holds this much device memory until the
  * process exits.
  */
-#define FA_BWD_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /*
  * fa_bwd without a workspace argument.  The paper and the pages have no
@@ -147,16 +143,17 @@ fa_status fa_check_error(fa_stream_t stream);
  * nothing: its workspace is a file-scope device array of
  * FA_BWD_NOALLOC_SCRATCH_BYTES bytes inside this library.
  *   - Size limit: returns FA_ERR_UNSUPPORTED, and enqueues nothing, when
- *     fa_bwd_workspace_bytes(B, H, N, d) exceeds FA_BWD_NOALLOC_SCRATCH_BYTES
- *     (for example B=16, H=16, N=512, d=64 fits; B=1, H=16, N=16384, d=128
- *     does not).
+ *     fa_bwd_workspace_bytes(B, H, N, d) exceeds FA_BWD_NOALLOC_SCRATCH_BYTES,
+ *     i.e. when B * H * N exceeds 4,194,304 rows (B=1, H=16, N=16384 fits;
+ *     B=8, H=64, N=8200 does not).
  *   - First call on a device: looks up the array's device address there
  *     (cudaGetSymbolAddress, which may load the library's device code on that
  *     device).  Make that first call before any stream capture.
  *   - Sharing: every call on a device uses the same array, which keeps the
- *     last call's contents; each call clears the part that must start at zero.
- *     Calls whose work overlaps on the GPU (different streams without ordering
- *     between them) race on the array and give wrong results -- order them.
+ *     last call's contents; each call overwrites what it reads before reading
+ *     it.  Calls whose work overlaps on the GPU (different streams without
+ *     ordering between them) race on the array and give wrong results --
+ *     order them.
  */
 fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                          const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
@@ -172,6 +169,13 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
  * the context stays usable.  Enqueues only; returns FA_OK once launched.
  */
 fa_status fa_selftest_stalled_wait(uint64_t limit_ns, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word (FA_ERR_TIMEOUT if a kernel gave up), or FA_ERR_CUDA if the stream
+ * itself reports an error.
+ */
+fa_status fa_check_error(fa_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status status);

@@ -32,9 +32,9 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_main",
-              "fa_bwd_finish", "fa_bwd_workspace_bytes", "fa_check_error", "fa_status_string",
-              "fa_selftest_stalled_wait"):
+    for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_dkdv",
+              "fa_bwd_dq", "fa_bwd_workspace_bytes", "fa_check_error", "fa_status_string",
+              "fa_selftest_stalled_wait", "fa_bwd_noalloc"):
         assert n in names
 
 
@@ -55,7 +55,7 @@ def test_workspace_size(lib):
     B, H, N, d = 2, 3, 100, 64
     rows = B * H * N
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == r256(rows * d * 4) + r256(rows * 4)
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == r256(rows * 4)
     assert fa.fa_bwd_workspace_bytes(B, H, N, 96) == 0
     assert fa.fa_bwd_workspace_bytes(0, H, N, d) == 0
 
@@ -94,6 +94,11 @@ def test_backward_stages_reject_invalid_arguments(lib):
     assert lib.fa_bwd_prepare(null, fake, 1, 1, 128, 64, fake, 1 << 20, null) == 1
     assert lib.fa_bwd_prepare(fake, fake, 1, 1, 128, 64, fake, 16, null) == 1
     assert lib.fa_bwd_prepare(fake, fake, 1, 1, 128, 96, fake, 1 << 20, null) == 2
-    assert lib.fa_bwd_main(*([fake] * 7), 1, 1, 128, 64, f(0.1), 0, null, ctypes.c_void_p(0x10010),
-                           1 << 20, null) == 1  # workspace not 256-byte aligned
-    assert lib.fa_bwd_finish(fake, 1, 1, 128, 64, f(0.1), null, 1 << 20, null) == 1
+    # workspace not 256-byte aligned
+    assert lib.fa_bwd_dkdv(*([fake] * 7), 1, 1, 128, 64, f(0.1), 0, null, ctypes.c_void_p(0x10010),
+                           1 << 20, null) == 1
+    assert lib.fa_bwd_dq(*([fake] * 5), null, 1, 1, 128, 64, f(0.1), 0, null, fake, 1 << 20,
+                         null) == 1
+    # the no-allocation variant validates sizes before touching its scratch
+    assert lib.fa_bwd_noalloc(*([fake] * 9), 1, 1, 128, 96, f(0.1), 0, null, null) == 2
+    assert lib.fa_bwd_noalloc(*([fake] * 9), 0, 1, 128, 64, f(0.1), 0, null, null) == 1

@@ -107,11 +107,10 @@ def test_sweep_sampled(d, N, causal):
     check_sampled(case, causal, [(B - 1, Hh - 1)], rows, rows)
 
 
-def test_deterministic_up_to_reduction_order():
-    # dQ accumulates with fp32 atomics (order may vary); dK and dV do not.
+def test_deterministic():
+    # no atomics anywhere in the backward pass: identical inputs give identical bits
     case = H.Case(1006, 2, 4, 700, 128)
     a = run_bwd(case, True)
     b = run_bwd(case, True)
-    np.testing.assert_array_equal(a[1], b[1])
-    np.testing.assert_array_equal(a[2], b[2])
-    assert H.err_rel(a[0], b[0]) <= 1e-2
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)

@@ -62,20 +62,21 @@ def test_noalloc_matches_fa_bwd_on_calls_in_a_row(lib):
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
             e = H.err_rel(H.to_f64(g), H.to_f64(r))
             assert e <= H.TOL_GRAD_REL, (name, case.N, causal, e)
-        # dK and dV do not depend on reduction order: they match bit for bit
-        np.testing.assert_array_equal(H.to_f64(got[1]), H.to_f64(ref[1]))
-        np.testing.assert_array_equal(H.to_f64(got[2]), H.to_f64(ref[2]))
+        # the backward pass is deterministic: the gradients match bit for bit
+        for g, r in zip(got, ref):
+            np.testing.assert_array_equal(H.to_f64(g), H.to_f64(r))
 
 
 def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
     import torch
     from exact_io_aware_40_gb300 import fa
-    B, Hh, N, d = 1, 16, 16384, 128
-    assert fa.fa_bwd_workspace_bytes(B, Hh, N, d) > 64 * 1024 * 1024
+    # 8 * 64 * 8200 = 4,198,400 rows of fp32 row terms: just over 16 MiB
+    B, Hh, N, d = 8, 64, 8200, 64
+    assert fa.fa_bwd_workspace_bytes(B, Hh, N, d) > 16 * 1024 * 1024
     x = torch.zeros(B, Hh, N, d, dtype=torch.bfloat16, device="cuda")
     L = torch.zeros(B, Hh, N, dtype=torch.float32, device="cuda")
     st = lib.fa_bwd_noalloc(_p(x), _p(x), _p(x), _p(x), _p(x), _p(L), _p(x), _p(x), _p(x),
-                            B, Hh, N, d, ctypes.c_float(0.088), 0, _p(None),
+                            B, Hh, N, d, ctypes.c_float(0.125), 0, _p(None),
                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == fa.FA_ERR_UNSUPPORTED
     fa.fa_check_error()
