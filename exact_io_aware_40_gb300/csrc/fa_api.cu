@@ -86,7 +86,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 fa_status check_common(int B, int H, int N, int d, float scale) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const long long tiles = (static_cast<long long>(N) + 127) / 128;
@@ -159,8 +159,8 @@ fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, flo
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
   if ((st = map_bf16(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tv, V, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, BH, fa::fwd_kv_rows(d))) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, BH, fa::fwd_kv_rows(d))) != FA_OK) return st;
   if ((st = map_bf16(enc, &to, O, d, N, BH, 128)) != FA_OK) return st;
   fa::FwdArgs a;
   a.L = L;
@@ -182,7 +182,7 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
   return round256(static_cast<size_t>(B) * H * N * sizeof(float));
 }
 
@@ -254,12 +254,13 @@ fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* d
   if (st != FA_OK) return st;
   a.dK = static_cast<uint16_t*>(dK);
   a.dV = static_cast<uint16_t*>(dV);
-  a.n_qtiles = (N + 63) / 64;
+  const int qrows = fa::bwd_dkdv_qrows(d);
+  a.n_qtiles = (N + qrows - 1) / qrows;
   CUtensorMap tq, tk, tv, tdo;
-  if ((st = map_bf16(enc, &tq, Q, d, N, a.BH, 64)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tq, Q, d, N, a.BH, qrows)) != FA_OK) return st;
   if ((st = map_bf16(enc, &tk, K, d, N, a.BH, 128)) != FA_OK) return st;
   if ((st = map_bf16(enc, &tv, V, d, N, a.BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tdo, dO, d, N, a.BH, 64)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tdo, dO, d, N, a.BH, qrows)) != FA_OK) return st;
   return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -276,8 +277,8 @@ fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO,
   a.n_qtiles = (N + 127) / 128;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if ((st = map_bf16(enc, &tq, Q, d, N, a.BH, 128)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tk, K, d, N, a.BH, 64)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tv, V, d, N, a.BH, 64)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, a.BH, fa::bwd_dq_krows(d))) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, a.BH, fa::bwd_dq_krows(d))) != FA_OK) return st;
   if ((st = map_bf16(enc, &tdo, dO, d, N, a.BH, 128)) != FA_OK) return st;
   if ((st = map_bf16(enc, &tdq, dQ, d, N, a.BH, 128)) != FA_OK) return st;
   return fa::launch_bwd_dq(d, tq, tk, tv, tdo, tdq, a, stream) == cudaSuccess ? FA_OK

@@ -67,22 +67,24 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t atom) {
 // dK, dV
 // ===========================================================================
 constexpr int kKeys = 128;  // keys per CTA (MMA M)
-constexpr int kQStep = 64;  // query rows per step
 
-template <int HD>
+// HD: head dim; DH: columns of dK/dV this CTA accumulates (HD, or HD/2 when
+// d = 256 and the two halves go to two CTAs); QS: query rows per step.
+template <int HD, int DH, int QS>
 struct KvCfg {
   static constexpr int kAtoms = HD / 64;
+  static constexpr int kHalves = HD / DH;
   static constexpr int kKVAtom = 128 * 128;          // 128 rows x 128 B
   static constexpr int kKVTile = kAtoms * kKVAtom;
-  static constexpr int kQAtom = kQStep * 128;        // 64 rows x 128 B
+  static constexpr int kQAtom = QS * 128;            // QS rows x 128 B
   static constexpr int kQTile = kAtoms * kQAtom;
-  static constexpr int kSt = 4;                      // Q/dO ring depth
+  static constexpr int kSt = HD == 256 ? 3 : 4;      // Q/dO ring depth
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKVTile;
   static constexpr int kOffQ = 2 * kKVTile;
   static constexpr int kOffdO = kOffQ + kSt * kQTile;
-  static constexpr int kOffLD = kOffdO + kSt * kQTile;   // kSt x (L2[64], D[64])
-  static constexpr int kOffBar = kOffLD + kSt * 512;
+  static constexpr int kOffLD = kOffdO + kSt * kQTile;   // kSt x (L2[QS], D[QS])
+  static constexpr int kOffBar = kOffLD + kSt * 8 * QS;
   // kv, qdo_full[kSt], qdo_empty[kSt], ld_full[kSt], s[2], dp[2], p[2], ds[2],
   // final, drain
   static constexpr int kNumBar = 1 + 3 * kSt + 8 + 2;
@@ -90,17 +92,18 @@ struct KvCfg {
   static constexpr int kUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kUsed + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // TMEM: warpgroup x owns S^T at 128x (P^T over its first 32 columns) and
-  // dP^T at 128x + 64 (dS^T over its first 32 columns); dV, dK at 256.
-  static constexpr uint32_t kColdV = 256, kColdK = 256 + HD;
+  // TMEM: warpgroup x owns S^T at 2 QS x (P^T over its first QS/2 columns)
+  // and dP^T at 2 QS x + QS (dS^T over its first QS/2 columns); dV, dK at 256.
+  static constexpr uint32_t kColdV = 256, kColdK = 256 + DH;
+  static_assert(4 * QS <= 256 && 256 + 2 * DH <= 512, "TMEM budget");
 };
 
-template <int HD>
+template <int HD, int DH, int QS>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const BwdArgs a) {
-  using C = KvCfg<HD>;
+  using C = KvCfg<HD, DH, QS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
@@ -124,14 +127,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Head-major order; small kt (most work under causal) first.
-  const int bh = static_cast<int>(blockIdx.x / a.n_ktiles);
-  const int kt = static_cast<int>(blockIdx.x % a.n_ktiles);
+  // Head-major order; small kt (most work under causal) first; the column
+  // halves of one key block (d = 256) are neighbours.
+  const int half = static_cast<int>(blockIdx.x % C::kHalves);
+  const int blk = static_cast<int>(blockIdx.x / C::kHalves);
+  const int bh = blk / a.n_ktiles;
+  const int kt = blk % a.n_ktiles;
   const int k0 = kt * kKeys;
   const int b = bh / a.H;
+  const int hatom = half * (DH / 64);  // first 64-column atom of this CTA's half
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const int i_start = a.causal ? k0 / kQStep : 0;
+  const int i_start = a.causal ? k0 / QS : 0;
   const int n_iter = (k0 >= kv_limit) ? 0 : a.n_qtiles - i_start;
 
   if (tid == 0) {
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < C::kSt; ++t) last[t] = -1;
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::kSt;
-        const int q0 = (i_start + it) * kQStep;
+        const int q0 = (i_start + it) * QS;
         if (it >= C::kSt &&
             !__all_sync(0xffffffffu, mbar_wait(bar_qdo_empty(st), ((it / C::kSt) & 1) ^ 1, ab)))
           break;
@@ -197,12 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         last[st] = it;
-        float* L2 = sLD + st * 128;
-        float* Dv = L2 + 64;
+        float* L2 = sLD + st * 2 * QS;
+        float* Dv = L2 + QS;
         const long long rbase = static_cast<long long>(bh) * a.N;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int r = lane * 2 + e;
+        for (int e = 0; e < QS / 32; ++e) {
+          const int r = lane * (QS / 32) + e;
           const int q = q0 + r;
           L2[r] = q < a.N ? a.L[rbase + q] * kLog2e : 0.f;
           Dv[r] = q < a.N ? a.D[rbase + q] : 0.f;
@@ -218,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_iter > 0) {
-      constexpr uint32_t idS = idesc_bf16(kKeys, kQStep, false, false);  // S^T, dP^T
-      constexpr uint32_t idKV = idesc_bf16(kKeys, HD, false, true);      // dV, dK
+      constexpr uint32_t idS = idesc_bf16(kKeys, QS, false, false);  // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16(kKeys, DH, false, true);  // dV, dK
       // S^T(i), dP^T(i) into warpgroup (i & 1)'s columns
       auto issue_s_dp = [&](int it) -> bool {
         const int st = it % C::kSt, x = it & 1;
@@ -228,12 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = sQ + st * C::kQTile, g = sdO + st * C::kQTile;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + 128u * x, kmaj(sK, k, C::kKVAtom), kmaj(q, k, C::kQAtom), idS,
+          mma_ss(tmem + 2u * QS * x, kmaj(sK, k, C::kKVAtom), kmaj(q, k, C::kQAtom), idS,
                  k > 0 ? 1u : 0u);
         mma_commit(bar_s(x));
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + 128u * x + 64, kmaj(sV, k, C::kKVAtom), kmaj(g, k, C::kQAtom), idS,
+          mma_ss(tmem + 2u * QS * x + QS, kmaj(sV, k, C::kKVAtom), kmaj(g, k, C::kQAtom), idS,
                  k > 0 ? 1u : 0u);
         mma_commit(bar_dp(x));
         return true;
@@ -249,9 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar_ds(y), (pv >> 1) & 1, ab))) break;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kQStep / 16; ++k)
-            mma_ts(tmem + C::kColdK, tmem + 128u * y + 64 + k * 8,
-                   mnmaj(sQ + st * C::kQTile, k, C::kQAtom), idKV, (pv > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < QS / 16; ++k)
+            mma_ts(tmem + C::kColdK, tmem + 2u * QS * y + QS + k * 8,
+                   mnmaj(sQ + st * C::kQTile + hatom * C::kQAtom, k, C::kQAtom), idKV,
+                   (pv > 0 || k > 0) ? 1u : 0u);
           mma_commit(bar_qdo_empty(st));
           // S^T(it+1) overwrites P^T(it-1) and dP^T(it+1) overwrites dS^T(it-1):
           // dV(it-1) and dK(it-1) were issued first (MMAs execute in order).
@@ -262,9 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar_p(x), (it >> 1) & 1, ab))) break;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kQStep / 16; ++k)
-            mma_ts(tmem + C::kColdV, tmem + 128u * x + k * 8, mnmaj(sdO + st * C::kQTile, k, C::kQAtom),
-                   idKV, (it > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < QS / 16; ++k)
+            mma_ts(tmem + C::kColdV, tmem + 2u * QS * x + k * 8,
+                   mnmaj(sdO + st * C::kQTile + hatom * C::kQAtom, k, C::kQAtom), idKV,
+                   (it > 0 || k > 0) ? 1u : 0u);
         }
       }
       mma_commit(bar_final);
@@ -278,24 +287,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kr = quarter * 32 + lane;   // key row = TMEM lane
     const int key = k0 + kr;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t cs = 128u * x, cdp = 128u * x + 64;
+    const uint32_t cs = 2u * QS * x, cdp = 2u * QS * x + QS;
     const bool key_ok = key < kv_limit;
     bool ok = true;
     for (int it = x, n = 0; it < n_iter; it += 2, ++n) {
       const int st = it % C::kSt;
-      const int q0 = (i_start + it) * kQStep;
-      const float* L2 = sLD + st * 128;
-      const float* Dv = L2 + 64;
+      const int q0 = (i_start + it) * QS;
+      const float* L2 = sLD + st * 2 * QS;
+      const float* Dv = L2 + QS;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_ld_full(st), (it / C::kSt) & 1, ab) &&
                                        mbar_wait(bar_s(x), n & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool need_mask = !key_ok || (q0 + kQStep > a.N) || (a.causal && q0 < k0 + kKeys - 1);
-      float p[64];
+      const bool need_mask = !key_ok || (q0 + QS > a.N) || (a.causal && q0 < k0 + kKeys - 1);
+      float p[QS];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < QS / 32; ++c) {
         uint32_t sr[32];
         tmem_ld32(tl + cs + 32 * c, sr);
         tmem_wait_ld();
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < QS / 32; ++c) {
         uint32_t dr[32];
         tmem_ld32(tl + cdp + 32 * c, dr);
         tmem_wait_ld();
@@ -355,11 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
       const bool store = key < a.N;
       const long long row = static_cast<long long>(bh) * a.N + (store ? key : 0);
-      uint16_t* dst = (x == 0 ? a.dV : a.dK) + row * HD;
+      uint16_t* dst = (x == 0 ? a.dV : a.dK) + row * HD + half * DH;
       const uint32_t col = x == 0 ? C::kColdV : C::kColdK;
       const float mul = x == 0 ? 1.f : a.scale;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         uint32_t r[32];
         if (n_iter > 0) {
           tmem_ld32(tl + col + 32 * c, r);
@@ -393,19 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dQ
 // ===========================================================================
 constexpr int kQRows = 128;  // query rows per block (MMA M)
-constexpr int kKStep = 64;   // keys per step
 
-template <int HD>
+// QT: query blocks per CTA (2, or 1 for d = 256); KS: keys per step.
+template <int HD, int QT, int KS>
 struct QCfg {
   static constexpr int kAtoms = HD / 64;
   static constexpr int kQAtom = kQRows * 128;       // 128 rows x 128 B
   static constexpr int kQTile = kAtoms * kQAtom;
-  static constexpr int kKAtom = kKStep * 128;       // 64 rows x 128 B
+  static constexpr int kKAtom = KS * 128;           // KS rows x 128 B
   static constexpr int kKTile = kAtoms * kKAtom;
   static constexpr int kSt = 3;                     // K/V ring depth
-  static constexpr int kOffQ = 0;                   // Q_A, Q_B
-  static constexpr int kOffdO = 2 * kQTile;         // dO_A, dO_B
-  static constexpr int kOffK = 4 * kQTile;
+  static constexpr int kOffQ = 0;                   // Q_A (, Q_B)
+  static constexpr int kOffdO = QT * kQTile;        // dO_A (, dO_B)
+  static constexpr int kOffK = 2 * QT * kQTile;
   static constexpr int kOffV = kOffK + kSt * kKTile;
   static constexpr int kOffBar = kOffV + kSt * kKTile;
   // q_full[2], kv_full[kSt], kv_empty[kSt], s[2], dp[2], ds[2], final[2], drain
@@ -414,17 +423,18 @@ struct QCfg {
   static constexpr int kUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kUsed + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // TMEM: block x owns S at 128x and dP at 128x + 64 (dS over its first 32
-  // columns); dQ_A, dQ_B at 256 and 256 + d.
+  // TMEM: block x owns S at 2 KS x and dP at 2 KS x + KS (dS over its first
+  // KS/2 columns); dQ_A (, dQ_B) at 256 (and 256 + d).
   static constexpr uint32_t kColdQ = 256;
+  static_assert(4 * KS <= 256 && 256 + QT * HD <= 512, "TMEM budget");
 };
 
-template <int HD>
+template <int HD, int QT, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
-  using C = QCfg<HD>;
+  using C = QCfg<HD, QT, KS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
@@ -447,18 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Head-major order with the longest query blocks (causal) of a head first.
-  const int n_pairs = (a.n_qtiles + 1) / 2;
+  const int n_pairs = (a.n_qtiles + QT - 1) / QT;
   const int bh = static_cast<int>(blockIdx.x / n_pairs);
   const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs);
-  const int qtA = 2 * pr;
+  const int qtA = QT * pr;
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const int kv_steps = (kv_limit + kKStep - 1) / kKStep;
-  const bool hasB = qtA + 1 < a.n_qtiles;
+  const int kv_steps = (kv_limit + KS - 1) / KS;
+  const bool hasB = QT == 2 && qtA + 1 < a.n_qtiles;
   // key steps each query block needs: keys <= last row of the block (causal)
-  const int TA = a.causal ? min(kv_steps, 2 * qtA + 2) : kv_steps;
-  const int TB = hasB ? (a.causal ? min(kv_steps, 2 * qtA + 4) : kv_steps) : 0;
+  const int TA = a.causal ? min(kv_steps, (qtA * kQRows + kQRows - 1) / KS + 1) : kv_steps;
+  const int TB =
+      hasB ? (a.causal ? min(kv_steps, ((qtA + 1) * kQRows + kQRows - 1) / KS + 1) : kv_steps) : 0;
   const int T = max(TA, TB);
 
   if (tid == 0) {
@@ -514,9 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= C::kSt && !mbar_wait(bar_kvempty(st), ((j / C::kSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_kvfull(st), 2 * C::kKTile);
         for (int c = 0; c < C::kAtoms; ++c) {
-          tma_load_3d(sK + st * C::kKTile + c * C::kKAtom, &tmK, c * 64, j * kKStep, bh,
+          tma_load_3d(sK + st * C::kKTile + c * C::kKAtom, &tmK, c * 64, j * KS, bh,
                       bar_kvfull(st), pol_kv);
-          tma_load_3d(sV + st * C::kKTile + c * C::kKAtom, &tmV, c * 64, j * kKStep, bh,
+          tma_load_3d(sV + st * C::kKTile + c * C::kKAtom, &tmV, c * 64, j * KS, bh,
                       bar_kvfull(st), pol_kv);
         }
         last[st] = j;
@@ -531,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0 && T > 0) {
-      constexpr uint32_t idS = idesc_bf16(kQRows, kKStep, false, false);  // S, dP
+      constexpr uint32_t idS = idesc_bf16(kQRows, KS, false, false);  // S, dP
       constexpr uint32_t idQ = idesc_bf16(kQRows, HD, false, true);       // dQ
       // S_x(j), dP_x(j) into block x's columns
       auto issue_s_dp = [&](int x, int j) -> bool {
@@ -543,11 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k = sK + st * C::kKTile, v = sV + st * C::kKTile;
 #pragma unroll
         for (int s = 0; s < HD / 16; ++s)
-          mma_ss(tmem + 128u * x, kmaj(q, s, C::kQAtom), kmaj(k, s, C::kKAtom), idS, s > 0 ? 1u : 0u);
+          mma_ss(tmem + 2u * KS * x, kmaj(q, s, C::kQAtom), kmaj(k, s, C::kKAtom), idS,
+                 s > 0 ? 1u : 0u);
         mma_commit(bar_s(x));
 #pragma unroll
         for (int s = 0; s < HD / 16; ++s)
-          mma_ss(tmem + 128u * x + 64, kmaj(g, s, C::kQAtom), kmaj(v, s, C::kKAtom), idS,
+          mma_ss(tmem + 2u * KS * x + KS, kmaj(g, s, C::kQAtom), kmaj(v, s, C::kKAtom), idS,
                  s > 0 ? 1u : 0u);
         mma_commit(bar_dp(x));
         return true;
@@ -564,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // dQ_x += dS_x K_j (A = dS from TMEM, B = K_j MN-major)
 #pragma unroll
-          for (int s = 0; s < kKStep / 16; ++s)
-            mma_ts(tmem + C::kColdQ + static_cast<uint32_t>(HD) * x, tmem + 128u * x + 64 + s * 8,
+          for (int s = 0; s < KS / 16; ++s)
+            mma_ts(tmem + C::kColdQ + static_cast<uint32_t>(HD) * x, tmem + 2u * KS * x + KS + s * 8,
                    mnmaj(sK + st * C::kKTile, s, C::kKAtom), idQ, (j > 0 || s > 0) ? 1u : 0u);
           if (j == Tx - 1) mma_commit(bar_final(x));
           // the last reader of K_j, V_j releases the stage
@@ -587,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q0 = (qtA + x) * kQRows;
     const int grow = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t cs = 128u * x, cdp = 128u * x + 64;
+    const uint32_t cs = 2u * KS * x, cdp = 2u * KS * x + KS;
     const uint32_t cq = C::kColdQ + static_cast<uint32_t>(HD) * x;
     const long long ridx = static_cast<long long>(bh) * a.N + grow;
     const float L2 = grow < a.N ? a.L[ridx] * kLog2e : 0.f;
@@ -599,15 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int key0 = j * kKStep;
-      const bool need_mask = (key0 + kKStep > kv_limit) || (a.causal && key0 + kKStep - 1 > q0);
-      uint32_t sr[2][32];
-      tmem_ld32(tl + cs, sr[0]);
-      tmem_ld32(tl + cs + 32, sr[1]);
-      tmem_wait_ld();
-      float p[64];
+      const int key0 = j * KS;
+      const bool need_mask = (key0 + KS > kv_limit) || (a.causal && key0 + KS - 1 > q0);
+      uint32_t sr[KS / 32][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < KS / 32; ++c) tmem_ld32(tl + cs + 32 * c, sr[c]);
+      tmem_wait_ld();
+      float p[KS];
+#pragma unroll
+      for (int c = 0; c < KS / 32; ++c) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float v = ex2(fmaf(__uint_as_float(sr[c][e]), a.scale_log2, -L2));
@@ -624,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < KS / 32; ++c) {
         uint32_t dr[32];
         tmem_ld32(tl + cdp + 32 * c, dr);
         tmem_wait_ld();
@@ -708,31 +720,33 @@ cudaError_t set_smem(Kern k, int bytes, bool (&done)[64]) {
   return cudaSuccess;
 }
 
-template <int HD>
+template <int HD, int DH, int QS>
 cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdArgs& a, cudaStream_t stream) {
+  using C = KvCfg<HD, DH, QS>;
   static bool done[64] = {};
-  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<HD>, KvCfg<HD>::kSmemBytes, done);
+  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<HD, DH, QS>, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(a.n_ktiles) * a.BH;
+  const long long grid = static_cast<long long>(a.n_ktiles) * a.BH * C::kHalves;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dkdv_kernel<HD><<<static_cast<unsigned>(grid), kThreads, KvCfg<HD>::kSmemBytes, stream>>>(
+  fa_bwd_dkdv_kernel<HD, DH, QS><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
       tmQ, tmK, tmV, tmdO, a);
   return cudaGetLastError();
 }
 
-template <int HD>
+template <int HD, int QT, int KS>
 cudaError_t launch_dq_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdArgs& a,
                         cudaStream_t stream) {
+  using C = QCfg<HD, QT, KS>;
   static bool done[64] = {};
-  cudaError_t e = set_smem(fa_bwd_dq_kernel<HD>, QCfg<HD>::kSmemBytes, done);
+  cudaError_t e = set_smem(fa_bwd_dq_kernel<HD, QT, KS>, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>((a.n_qtiles + 1) / 2) * a.BH;
+  const long long grid = static_cast<long long>((a.n_qtiles + QT - 1) / QT) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dq_kernel<HD><<<static_cast<unsigned>(grid), kThreads, QCfg<HD>::kSmemBytes, stream>>>(
+  fa_bwd_dq_kernel<HD, QT, KS><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
       tmQ, tmK, tmV, tmdO, tmdQ, a);
   return cudaGetLastError();
 }
@@ -743,8 +757,9 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tmQ, const CUtensorMap& tm
                             const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdArgs& a,
                             cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dkdv_t<64>(tmQ, tmK, tmV, tmdO, a, stream);
-    case 128: return launch_dkdv_t<128>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 64: return launch_dkdv_t<64, 64, 64>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 128: return launch_dkdv_t<128, 128, 64>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 256: return launch_dkdv_t<256, 128, 32>(tmQ, tmK, tmV, tmdO, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -753,8 +768,9 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                           const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dq_t<64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
-    case 128: return launch_dq_t<128>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 64: return launch_dq_t<64, 2, 64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 128: return launch_dq_t<128, 2, 64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 256: return launch_dq_t<256, 1, 32>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

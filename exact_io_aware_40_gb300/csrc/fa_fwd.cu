@@ -449,6 +449,7 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
   switch (d) {
     case 64: return launch_fwd_t<64>(tmQ, tmK, tmV, tmO, a, stream);
     case 128: return launch_fwd_t<128>(tmQ, tmK, tmV, tmO, a, stream);
+    case 256: return launch_fwd_d256(tmQ, tmK, tmV, tmO, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

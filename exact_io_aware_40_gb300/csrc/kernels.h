@@ -22,6 +22,13 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream);
 
+// Forward for d = 256 (one 128-row query block per CTA, 64-key blocks; the
+// K and V maps use 64-row boxes).  grid = ceil(N/128) * BH.
+cudaError_t launch_fwd_d256(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
+                            cudaStream_t stream);
+inline int fwd_kv_rows(int d) { return d == 256 ? 64 : 128; }
+
 struct BwdPreArgs {
   const uint16_t* O;    // bf16 [BH, N, d]
   const uint16_t* dO;   // bf16 [BH, N, d]
@@ -46,13 +53,19 @@ struct BwdArgs {
   int causal;
 };
 
-// dK, dV: grid = ceil(N/128) * BH.  Q and dO maps use 64-row boxes, K and V
-// 128-row boxes.
+// Query rows per step of the dK/dV kernel (the box height of its Q and dO
+// maps) and keys per step of the dQ kernel (the box height of its K and V maps).
+inline int bwd_dkdv_qrows(int d) { return d == 256 ? 32 : 64; }
+inline int bwd_dq_krows(int d) { return d == 256 ? 32 : 64; }
+
+// dK, dV: grid = ceil(N/128) * BH * (d == 256 ? 2 : 1) (d = 256: one CTA per
+// 128-column half of dK, dV).  Q and dO maps use bwd_dkdv_qrows(d)-row boxes,
+// K and V 128-row boxes.
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdArgs& a,
                             cudaStream_t stream);
-// dQ: grid = ceil(N/256) * BH.  Q, dO and dQ maps use 128-row boxes, K and V
-// 64-row boxes.
+// dQ: grid = ceil(N/256) * BH (d = 256: ceil(N/128) * BH).  Q, dO and dQ maps
+// use 128-row boxes, K and V bwd_dq_krows(d)-row boxes.
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                           const BwdArgs& a, cudaStream_t stream);

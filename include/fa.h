@@ -20,7 +20,7 @@
  *   - Q, K, V, O, dO, dQ, dK, dV: bf16, contiguous [B, H, N, d] (d fastest),
  *     DEVICE pointers, 16-byte aligned.  L and the workspace's statistics are
  *     fp32; L is [B, H, N].
- *   - d must be 64 or 128; B, H, N >= 1; B*H*ceil(N/128) < 2^31 (element
+ *   - d must be 64, 128 or 256; B, H, N >= 1; B*H*ceil(N/128) < 2^31 (element
  *     offsets are 64-bit, so tensors may exceed 2^31 elements).
  *   - scale multiplies Q K^T before the mask and the softmax (usually 1/sqrt(d));
  *     it must be finite and > 0.

@@ -59,14 +59,14 @@ def test_tiny_config(causal):
     check_full(H.Case(1000, 1, 2, 128, 64), causal)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 2, 63, 127, 129, 200, 383])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_lengths(d, N, causal):
     check_full(H.Case(4000 + N, 2, 2, N, d), causal)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_key_padding_edges(d, causal):
     case = H.Case(5000, 4, 2, 300, d)
@@ -97,7 +97,7 @@ def test_long_sequence_sampled(causal):
     check_sampled(case, causal, [(0, 3)], rows, rows)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [512, 1024, 2048, 4096, 8192, 16384])
 @pytest.mark.parametrize("causal", [False, True])
 def test_sweep_sampled(d, N, causal):

@@ -60,14 +60,14 @@ def test_tiny_config(causal):
     check_full(H.Case(1000, 1, 2, 128, 64), causal)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 2, 63, 127, 129, 200, 383, 520])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_lengths(d, N, causal):
     check_full(H.Case(2000 + N, 2, 2, N, d), causal)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_key_padding_edges(d, causal):
     # empty rows (length 0), a single key, a tail crossing a tile, full length
@@ -102,7 +102,7 @@ def test_long_sequence_sampled_rows(causal):
     check_rows(case, causal, [(0, 0), (0, 7), (0, 15)], LONG_ROWS)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [512, 1024, 2048, 4096, 8192, 16384])
 @pytest.mark.parametrize("causal", [False, True])
 def test_sweep_sampled_rows(d, N, causal):
