@@ -68,7 +68,7 @@ def load_peaks():
 
 def kernel_digest():
     h = hashlib.sha256()
-    for name in ("fa_bwd.cu", "ptx.cuh", "kernels.h"):
+    for name in ("fa_bwd.cu", "fa_bwd_wide.cu", "ptx.cuh", "kernels.h"):
         with open(os.path.join(ROOT, "exact_io_aware_40_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -757,8 +757,8 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tmQ, const CUtensorMap& tm
                             const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdArgs& a,
                             cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dkdv_t<64, 64, 64>(tmQ, tmK, tmV, tmdO, a, stream);
-    case 128: return launch_dkdv_t<128, 128, 64>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 64:
+    case 128: return launch_bwd_dkdv_wide(d, tmQ, tmK, tmV, tmdO, a, stream);
     case 256: return launch_dkdv_t<256, 128, 32>(tmQ, tmK, tmV, tmdO, a, stream);
     default: return cudaErrorInvalidValue;
   }
@@ -768,8 +768,8 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                           const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dq_t<64, 2, 64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
-    case 128: return launch_dq_t<128, 2, 64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 64:
+    case 128: return launch_bwd_dq_wide(d, tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
     case 256: return launch_dq_t<256, 1, 32>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
     default: return cudaErrorInvalidValue;
   }

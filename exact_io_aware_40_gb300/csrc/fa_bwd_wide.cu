@@ -1,0 +1,745 @@
+// fa_bwd_wide.cu -- backward pass of exact attention for d = 64 and d = 128.
+//
+// Same method and formulas as fa_bwd.cu (P recomputed from L; dV = P^T dO,
+// dP = dO V^T, dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q; fmread.com
+// summary, section 三.2 "反向传播优化"), organised so that every tcgen05 product
+// is 128 wide (M = 128, N = 128): a product with N = 64 and both operands in
+// shared memory needs 192 B/clock of shared-memory bandwidth at full tensor
+// rate, more than an SM has, so it runs at two thirds of the rate at best;
+// N = 128 needs 128 B/clock (operands in shared memory) or 64 B/clock (A in
+// TMEM).  Each 128-wide step is split by columns between two softmax
+// warpgroups, so both work on every step in parallel:
+//
+// fa_bwd_dkdv_wide_kernel -- one CTA per 128-key block j, 128-row query steps
+//   i.  TMEM: S^T 0-127, dP^T 128-255 (keys on lanes, queries on columns), dV
+//   256.., dK 256+d.  Warpgroup A handles query columns 0-63 of the step,
+//   warpgroup B 64-127; each writes its P^T (bf16) over the first half of its
+//   own S^T columns and its dS^T over the first half of its own dP^T columns,
+//   and the dV and dK products address those halves k-step by k-step.
+//   Issue order per step: dV_i, S^T_{i+1} (after dV_i has read P^T_i),
+//   dK_i, dP^T_{i+1} (after dK_i has read dS^T_i).
+// fa_bwd_dq_wide_kernel -- one CTA per 128-row query block, 128-key steps j.
+//   TMEM: two S buffers 0-127 and 128-255 (S_{j+1} is computed while the
+//   warpgroups work on S_j), dP 256-383 (dS over its column halves as above),
+//   dQ 384... Warpgroup A handles key columns 0-63, B 64-127.  Issue order per
+//   step: dQ_j (after dS_j), dP_{j+1}, S_{j+2}.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kT = 128;  // keys per block = query rows per step (and vice versa)
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ bool bar_and_w(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_sync_w(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// K-major operand (128-row tile, 64-column atoms of 16 KB): step k covers
+// columns [16k, 16k+16) of d.
+__device__ __forceinline__ uint64_t kmaj128(uint32_t base, int k) {
+  return sdesc_sw128(base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+}
+// MN-major operand (128-row tile; rows = reduction dim): step k covers rows
+// [16k, 16k+16).
+__device__ __forceinline__ uint64_t mnmaj128(uint32_t base, int k) {
+  return sdesc_sw128(base + k * 2048, 16384, 1024);
+}
+// TMEM column of k-step k (16 rows of the reduction dim) of a bf16 A operand
+// whose two 64-row halves sit at `lo` and `hi`.
+__device__ __forceinline__ uint32_t split_col(uint32_t lo, uint32_t hi, int k) {
+  return k < 4 ? lo + 8u * k : hi + 8u * (k - 4);
+}
+
+template <int HD>
+struct WCfg {
+  static constexpr int kAtoms = HD / 64;
+  static constexpr int kTile = kAtoms * 16384;          // 128 rows x d bf16
+  static constexpr int kSt = HD == 64 ? 3 : 2;          // ring depth
+};
+
+// ===========================================================================
+// dK, dV
+// ===========================================================================
+template <int HD>
+struct KvW {
+  using W = WCfg<HD>;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = W::kTile;
+  static constexpr int kOffQ = 2 * W::kTile;                    // kSt stages
+  static constexpr int kOffdO = kOffQ + W::kSt * W::kTile;      // kSt stages
+  static constexpr int kLdSt = 4;                               // L, D ring depth
+  static constexpr int kOffLD = kOffdO + W::kSt * W::kTile;     // kLdSt x (L2[128], D[128])
+  static constexpr int kOffBar = kOffLD + kLdSt * 1024;
+  // kv, qdo_full[], qdo_empty[], ld_full[4], ld_empty[4], s, dp, p, ds, final, drain
+  static constexpr int kNumBar = 1 + 2 * W::kSt + 2 * kLdSt + 6;
+  static constexpr int kOffMisc = kOffBar + kNumBar * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + HD;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dkdv_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV,
+                            const __grid_constant__ CUtensorMap tmdO, const BwdArgs a) {
+  using C = KvW<HD>;
+  using W = WCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw_u32 + pad;
+
+  const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV, sQ = sb + C::kOffQ, sdO = sb + C::kOffdO;
+  float* sLD = reinterpret_cast<float*>(smem + C::kOffLD);
+  const uint32_t bar0 = sb + C::kOffBar;
+  const uint32_t bar_kv = bar0;
+  auto bar_qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (1 + W::kSt + s); };
+  auto bar_ld_full = [&](int s) { return bar0 + 8u * (1 + 2 * W::kSt + s); };
+  auto bar_ld_empty = [&](int s) { return bar0 + 8u * (1 + 2 * W::kSt + C::kLdSt + s); };
+  const uint32_t bar_s = bar0 + 8u * (1 + 2 * W::kSt + 2 * C::kLdSt);
+  const uint32_t bar_dp = bar_s + 8, bar_p = bar_s + 16, bar_ds = bar_s + 24;
+  const uint32_t bar_final = bar_s + 32, bar_drain = bar_s + 40;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Head-major order; small kt (most work under causal) first.
+  const int bh = static_cast<int>(blockIdx.x / a.n_ktiles);
+  const int kt = static_cast<int>(blockIdx.x % a.n_ktiles);
+  const int k0 = kt * kT;
+  const int b = bh / a.H;
+  int kv_limit = a.N;
+  if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
+  const int i_start = a.causal ? kt : 0;
+  const int n_iter = (k0 >= kv_limit) ? 0 : a.n_qtiles - i_start;
+
+  if (tid == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < W::kSt; ++s) {
+      mbar_init(bar_qdo_full(s), 1);
+      mbar_init(bar_qdo_empty(s), 1);
+    }
+    for (int s = 0; s < C::kLdSt; ++s) {
+      mbar_init(bar_ld_full(s), 32);
+      mbar_init(bar_ld_empty(s), 8);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_p, 8);
+    mbar_init(bar_ds, 8);
+    mbar_init(bar_final, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{a.err, abort_flag};
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer
+    if (n_iter > 0) {
+      uint64_t pol_kv = 0, pol_q = 0;
+      if (lane == 0) {
+        pol_kv = policy_evict_first();
+        pol_q = policy_evict_last();  // Q_i, dO_i are re-read by every key block
+        mbar_arrive_expect_tx(bar_kv, 2 * W::kTile);
+        for (int c = 0; c < W::kAtoms; ++c) {
+          tma_load_3d(sK + c * 16384, &tmK, c * 64, k0, bh, bar_kv, pol_kv);
+          tma_load_3d(sV + c * 16384, &tmV, c * 64, k0, bh, bar_kv, pol_kv);
+        }
+      }
+      int last[W::kSt];
+      for (int t = 0; t < W::kSt; ++t) last[t] = -1;
+      for (int it = 0; it < n_iter; ++it) {
+        const int st = it % W::kSt;
+        const int q0 = (i_start + it) * kT;
+        if (it >= W::kSt &&
+            !__all_sync(0xffffffffu, mbar_wait(bar_qdo_empty(st), ((it / W::kSt) & 1) ^ 1, ab)))
+          break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_qdo_full(st), 2 * W::kTile);
+          for (int c = 0; c < W::kAtoms; ++c) {
+            tma_load_3d(sQ + st * W::kTile + c * 16384, &tmQ, c * 64, q0, bh, bar_qdo_full(st),
+                        pol_q);
+            tma_load_3d(sdO + st * W::kTile + c * 16384, &tmdO, c * 64, q0, bh,
+                        bar_qdo_full(st), pol_q);
+          }
+        }
+        last[st] = it;
+      }
+      if (lane == 0 && *abort_flag) {
+        mbar_wait_drain(bar_kv, 0);
+        for (int s = 0; s < W::kSt; ++s)
+          if (last[s] >= 0) mbar_wait_drain(bar_qdo_full(s), (last[s] / W::kSt) & 1);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------ row terms L, D
+    // Off the Q/dO ring, up to kLdSt steps ahead of the softmax warpgroups.
+    const long long rbase = static_cast<long long>(bh) * a.N;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % C::kLdSt;
+      const int q0 = (i_start + it) * kT;
+      if (it >= C::kLdSt &&
+          !__all_sync(0xffffffffu, mbar_wait(bar_ld_empty(st), ((it / C::kLdSt) & 1) ^ 1, ab)))
+        break;
+      float* L2 = sLD + st * 256;
+      float* Dv = L2 + 128;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = lane * 4 + e;
+        const int q = q0 + r;
+        L2[r] = q < a.N ? a.L[rbase + q] * kLog2e : 0.f;
+        Dv[r] = q < a.N ? a.D[rbase + q] : 0.f;
+      }
+      mbar_arrive(bar_ld_full(st));
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t idS = idesc_bf16(kT, kT, false, false);  // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16(kT, HD, false, true);  // dV, dK
+      auto issue_s = [&](int it) {
+        const uint32_t q = sQ + (it % W::kSt) * W::kTile;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tmem + C::kColS, kmaj128(sK, k), kmaj128(q, k), idS, k > 0 ? 1u : 0u);
+        mma_commit(bar_s);
+      };
+      auto issue_dp = [&](int it) {
+        const uint32_t g = sdO + (it % W::kSt) * W::kTile;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tmem + C::kColdP, kmaj128(sV, k), kmaj128(g, k), idS, k > 0 ? 1u : 0u);
+        mma_commit(bar_dp);
+      };
+      bool ok = mbar_wait(bar_kv, 0, ab) && mbar_wait(bar_qdo_full(0), 0, ab);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int st = it % W::kSt;
+        const bool more = it + 1 < n_iter;
+        // dV += P^T dO_i (P^T halves at columns 0 and 64)
+        if (!(ok = mbar_wait(bar_p, it & 1, ab))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kT / 16; ++k)
+          mma_ts(tmem + C::kColdV, tmem + split_col(C::kColS, C::kColS + 64, k),
+                 mnmaj128(sdO + st * W::kTile, k), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        // S^T(i+1) overwrites P^T(i): the product above reads it first.
+        if (more) {
+          if (!(ok = mbar_wait(bar_qdo_full((it + 1) % W::kSt), ((it + 1) / W::kSt) & 1, ab)))
+            break;
+          tc_fence_after();
+          issue_s(it + 1);
+        }
+        // dK += dS^T Q_i (dS^T halves at columns 128 and 192)
+        if (!(ok = mbar_wait(bar_ds, it & 1, ab))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kT / 16; ++k)
+          mma_ts(tmem + C::kColdK, tmem + split_col(C::kColdP, C::kColdP + 64, k),
+                 mnmaj128(sQ + st * W::kTile, k), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        mma_commit(bar_qdo_empty(st));
+        // dP^T(i+1) overwrites dS^T(i): dK above reads it first.
+        if (more) issue_dp(it + 1);
+      }
+      mma_commit(bar_final);
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int x = (warp >> 2) - 1;        // 0: query columns 0-63, 1: 64-127
+    const int quarter = warp & 3;
+    const int kr = quarter * 32 + lane;   // key row = TMEM lane
+    const int key = k0 + kr;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t cs = C::kColS + 64u * x, cdp = C::kColdP + 64u * x;
+    const bool key_ok = key < kv_limit;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int lst = it % C::kLdSt;
+      const int q0 = (i_start + it) * kT + 64 * x;  // first query column of this half
+      const float* L2 = sLD + lst * 256 + 64 * x;
+      const float* Dv = sLD + lst * 256 + 128 + 64 * x;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_ld_full(lst), (it / C::kLdSt) & 1, ab) &&
+                                       mbar_wait(bar_s, it & 1, ab))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool need_mask = !key_ok || (q0 + 64 > a.N) || (a.causal && q0 < k0 + kT - 1);
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(tl + cs + 32 * c, sr);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qa = 32 * c + e;
+          float v = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -L2[qa]));
+          if (need_mask) {
+            const int qg = q0 + qa;
+            if (!key_ok || qg >= a.N || (a.causal && key > qg)) v = 0.f;
+          }
+          p[qa] = v;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
+        // P^T over columns this thread has read (first half of its S^T columns)
+        tmem_st16(tl + cs + 16 * c, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, it & 1, ab))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dr[32];
+        tmem_ld32(tl + cdp + 32 * c, dr);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int qa = 32 * c + 2 * e;
+          const float d0 = p[qa] * (__uint_as_float(dr[2 * e]) - Dv[qa]);
+          const float d1 = p[qa + 1] * (__uint_as_float(dr[2 * e + 1]) - Dv[qa + 1]);
+          w[e] = pack_bf16(d0, d1);
+        }
+        tmem_st16(tl + cdp + 16 * c, w);  // dS^T over columns this thread has read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_ds);
+        mbar_arrive(bar_ld_empty(lst));  // this step's L, D have been read
+      }
+    }
+    if (ok && n_iter > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_final, 0, ab));
+      tc_fence_after();
+    }
+    ok = bar_and_w(1 + x, 128, ok && *abort_flag == 0);
+    if (ok) {
+      // ------------------------------------------------------------ dV (A), dK (B)
+      // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
+      const bool store = key < a.N;
+      const long long row = static_cast<long long>(bh) * a.N + (store ? key : 0);
+      uint16_t* dst = (x == 0 ? a.dV : a.dK) + row * HD;
+      const uint32_t col = x == 0 ? C::kColdV : C::kColdK;
+      const float mul = x == 0 ? 1.f : a.scale;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t r[32];
+        if (n_iter > 0) {
+          tmem_ld32(tl + col + 32 * c, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(r[8 * t + 0]) * mul, __uint_as_float(r[8 * t + 1]) * mul);
+          v.y = pack_bf16(__uint_as_float(r[8 * t + 2]) * mul, __uint_as_float(r[8 * t + 3]) * mul);
+          v.z = pack_bf16(__uint_as_float(r[8 * t + 4]) * mul, __uint_as_float(r[8 * t + 5]) * mul);
+          v.w = pack_bf16(__uint_as_float(r[8 * t + 6]) * mul, __uint_as_float(r[8 * t + 7]) * mul);
+          if (store) *reinterpret_cast<uint4*>(dst + 32 * c + 8 * t) = v;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+template <int HD>
+struct QW {
+  using W = WCfg<HD>;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffdO = W::kTile;
+  static constexpr int kOffK = 2 * W::kTile;                 // kSt stages
+  static constexpr int kOffV = kOffK + W::kSt * W::kTile;    // kSt stages
+  static constexpr int kOffBar = kOffV + W::kSt * W::kTile;
+  // q_full, kv_full[], kv_empty[], s[2], dp, ds, final, drain
+  static constexpr int kNumBar = 1 + 2 * W::kSt + 6;
+  static constexpr int kOffMisc = kOffBar + kNumBar * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kColS = 0, kColdP = 256, kColdQ = 384;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ CUtensorMap tmdO,
+                          const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
+  using C = QW<HD>;
+  using W = WCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw_u32 + pad;
+
+  const uint32_t sQ = sb + C::kOffQ, sdO = sb + C::kOffdO, sK = sb + C::kOffK, sV = sb + C::kOffV;
+  const uint32_t bar0 = sb + C::kOffBar;
+  const uint32_t bar_q = bar0;
+  auto bar_kvfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_kvempty = [&](int s) { return bar0 + 8u * (1 + W::kSt + s); };
+  const uint32_t barx = bar0 + 8u * (1 + 2 * W::kSt);
+  auto bar_s = [&](int b2) { return barx + 8u * b2; };
+  const uint32_t bar_dp = barx + 16, bar_ds = barx + 24, bar_final = barx + 32, bar_drain = barx + 40;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Head-major order with the longest query blocks (causal) of a head first.
+  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
+  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
+  const int q0 = qt * kT;
+  const int b = bh / a.H;
+  int kv_limit = a.N;
+  if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
+  int T = (kv_limit + kT - 1) / kT;
+  if (a.causal) T = min(T, qt + 1);
+
+  if (tid == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < W::kSt; ++s) {
+      mbar_init(bar_kvfull(s), 1);
+      mbar_init(bar_kvempty(s), 1);
+    }
+    mbar_init(bar_s(0), 1);
+    mbar_init(bar_s(1), 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_ds, 8);
+    mbar_init(bar_final, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmdQ);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{a.err, abort_flag};
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer
+    if (lane == 0 && T > 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(bar_q, 2 * W::kTile);
+      for (int c = 0; c < W::kAtoms; ++c) {
+        tma_load_3d(sQ + c * 16384, &tmQ, c * 64, q0, bh, bar_q, pol_q);
+        tma_load_3d(sdO + c * 16384, &tmdO, c * 64, q0, bh, bar_q, pol_q);
+      }
+      int last[W::kSt];
+      for (int s = 0; s < W::kSt; ++s) last[s] = -1;
+      for (int j = 0; j < T; ++j) {
+        const int st = j % W::kSt;
+        if (j >= W::kSt && !mbar_wait(bar_kvempty(st), ((j / W::kSt) & 1) ^ 1, ab)) break;
+        mbar_arrive_expect_tx(bar_kvfull(st), 2 * W::kTile);
+        for (int c = 0; c < W::kAtoms; ++c) {
+          tma_load_3d(sK + st * W::kTile + c * 16384, &tmK, c * 64, j * kT, bh, bar_kvfull(st),
+                      pol_kv);
+          tma_load_3d(sV + st * W::kTile + c * 16384, &tmV, c * 64, j * kT, bh, bar_kvfull(st),
+                      pol_kv);
+        }
+        last[st] = j;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(bar_q, 0);
+        for (int s = 0; s < W::kSt; ++s)
+          if (last[s] >= 0) mbar_wait_drain(bar_kvfull(s), (last[s] / W::kSt) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idS = idesc_bf16(kT, kT, false, false);  // S, dP
+      constexpr uint32_t idQ = idesc_bf16(kT, HD, false, true);   // dQ
+      // S_j = Q K_j^T into buffer j & 1
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % W::kSt;
+        if (!mbar_wait(bar_kvfull(st), (j / W::kSt) & 1, ab)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tmem + C::kColS + 128u * (j & 1), kmaj128(sQ, k), kmaj128(sK + st * W::kTile, k),
+                 idS, k > 0 ? 1u : 0u);
+        mma_commit(bar_s(j & 1));
+        return true;
+      };
+      // dP_j = dO V_j^T (its stage was waited for by issue_s(j))
+      auto issue_dp = [&](int j) {
+        const int st = j % W::kSt;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tmem + C::kColdP, kmaj128(sdO, k), kmaj128(sV + st * W::kTile, k), idS,
+                 k > 0 ? 1u : 0u);
+        mma_commit(bar_dp);
+      };
+      bool ok = mbar_wait(bar_q, 0, ab);
+      if (ok) ok = issue_s(0);
+      if (ok) issue_dp(0);
+      if (ok && T > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < T; ++j) {
+        const int st = j % W::kSt;
+        if (!(ok = mbar_wait(bar_ds, j & 1, ab))) break;
+        tc_fence_after();
+        // dQ += dS K_j (dS halves at columns 256 and 320; B = K_j MN-major)
+#pragma unroll
+        for (int k = 0; k < kT / 16; ++k)
+          mma_ts(tmem + C::kColdQ, tmem + split_col(C::kColdP, C::kColdP + 64, k),
+                 mnmaj128(sK + st * W::kTile, k), idQ, (j > 0 || k > 0) ? 1u : 0u);
+        if (j == T - 1) mma_commit(bar_final);
+        mma_commit(bar_kvempty(st));
+        // dP_{j+1} overwrites dS_j (read by the product above: in-order);
+        // S_{j+2} takes the buffer of S_j, which the warpgroups have read.
+        if (j + 1 < T) issue_dp(j + 1);
+        if (j + 2 < T && !(ok = issue_s(j + 2))) break;
+      }
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int x = (warp >> 2) - 1;        // 0: key columns 0-63, 1: 64-127
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // query row = TMEM lane
+    const int grow = q0 + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t cdp = C::kColdP + 64u * x;
+    const long long ridx = static_cast<long long>(bh) * a.N + grow;
+    const float L2 = grow < a.N ? a.L[ridx] * kLog2e : 0.f;
+    const float Dr = grow < a.N ? a.D[ridx] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s(j & 1), (j >> 1) & 1, ab))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int key0 = j * kT + 64 * x;  // first key column of this half
+      const bool need_mask = (key0 + 64 > kv_limit) || (a.causal && key0 + 63 > q0);
+      uint32_t sr[2][32];
+      tmem_ld32(tl + C::kColS + 128u * (j & 1) + 64u * x, sr[0]);
+      tmem_ld32(tl + C::kColS + 128u * (j & 1) + 64u * x + 32, sr[1]);
+      tmem_wait_ld();
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float v = ex2(fmaf(__uint_as_float(sr[c][e]), a.scale_log2, -L2));
+          if (need_mask) {
+            const int key = key0 + 32 * c + e;
+            if (key >= kv_limit || (a.causal && key > grow)) v = 0.f;
+          }
+          p[32 * c + e] = v;
+        }
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, j & 1, ab))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dr[32];
+        tmem_ld32(tl + cdp + 32 * c, dr);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float d0 = p[32 * c + 2 * e] * (__uint_as_float(dr[2 * e]) - Dr);
+          const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - Dr);
+          w[e] = pack_bf16(d0, d1);
+        }
+        tmem_st16(tl + cdp + 16 * c, w);  // dS over columns this thread has read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
+    }
+    if (ok && T > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_final, 0, ab));
+      tc_fence_after();
+    }
+    // Both warpgroups agree (named barrier 1 over all 256 softmax threads).
+    ok = bar_and_w(1, 256, ok && *abort_flag == 0);
+    if (ok && x == 0) {
+      // ------------------------------------------------------------ epilogue
+      // dQ * scale -> bf16 -> the idle Q tile (swizzled like TMA) -> TMA store
+      // (rows >= N are clipped).  Every lane takes part in the loads.
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t r[32];
+        if (T > 0) {
+          tmem_ld32(tl + C::kColdQ + 32 * c, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        const int atom = (32 * c) / 64;
+        const int chunk0 = ((32 * c) % 64) / 8;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(r[8 * t + 0]) * a.scale, __uint_as_float(r[8 * t + 1]) * a.scale);
+          v.y = pack_bf16(__uint_as_float(r[8 * t + 2]) * a.scale, __uint_as_float(r[8 * t + 3]) * a.scale);
+          v.z = pack_bf16(__uint_as_float(r[8 * t + 4]) * a.scale, __uint_as_float(r[8 * t + 5]) * a.scale);
+          v.w = pack_bf16(__uint_as_float(r[8 * t + 6]) * a.scale, __uint_as_float(r[8 * t + 7]) * a.scale);
+          const int phys = (chunk0 + t) ^ (row & 7);
+          *reinterpret_cast<uint4*>(smem + C::kOffQ + atom * 16384 + row * 128 + phys * 16) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      bar_sync_w(2, 128);
+      if (quarter == 0 && lane == 0) {
+        for (int c = 0; c < W::kAtoms; ++c) tma_store_3d(&tmdQ, sQ + c * 16384, c * 64, q0, bh);
+        bulk_commit();
+        bulk_wait0();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename Kern>
+cudaError_t set_smem_w(Kern k, int bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !done[dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+template <int HD>
+cudaError_t launch_dkdv_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap& tmdO, const BwdArgs& a, cudaStream_t stream) {
+  static bool done[64] = {};
+  cudaError_t e = set_smem_w(fa_bwd_dkdv_wide_kernel<HD>, KvW<HD>::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(a.n_ktiles) * a.BH;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fa_bwd_dkdv_wide_kernel<HD><<<static_cast<unsigned>(grid), kThreads, KvW<HD>::kSmemBytes,
+                                stream>>>(tmQ, tmK, tmV, tmdO, a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_dq_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdArgs& a,
+                        cudaStream_t stream) {
+  static bool done[64] = {};
+  cudaError_t e = set_smem_w(fa_bwd_dq_wide_kernel<HD>, QW<HD>::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fa_bwd_dq_wide_kernel<HD><<<static_cast<unsigned>(grid), kThreads, QW<HD>::kSmemBytes,
+                              stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dkdv_wide(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                 const BwdArgs& a, cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch_dkdv_w<64>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 128: return launch_dkdv_w<128>(tmQ, tmK, tmV, tmdO, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_dq_wide(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                               const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                               const CUtensorMap& tmdQ, const BwdArgs& a, cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch_dq_w<64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 128: return launch_dq_w<128>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

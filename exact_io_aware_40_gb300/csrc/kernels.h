@@ -55,8 +55,8 @@ struct BwdArgs {
 
 // Query rows per step of the dK/dV kernel (the box height of its Q and dO
 // maps) and keys per step of the dQ kernel (the box height of its K and V maps).
-inline int bwd_dkdv_qrows(int d) { return d == 256 ? 32 : 64; }
-inline int bwd_dq_krows(int d) { return d == 256 ? 32 : 64; }
+inline int bwd_dkdv_qrows(int d) { return d == 256 ? 32 : 128; }
+inline int bwd_dq_krows(int d) { return d == 256 ? 32 : 128; }
 
 // dK, dV: grid = ceil(N/128) * BH * (d == 256 ? 2 : 1) (d = 256: one CTA per
 // 128-column half of dK, dV).  Q and dO maps use bwd_dkdv_qrows(d)-row boxes,
@@ -64,7 +64,14 @@ inline int bwd_dq_krows(int d) { return d == 256 ? 32 : 64; }
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdArgs& a,
                             cudaStream_t stream);
-// dQ: grid = ceil(N/256) * BH (d = 256: ceil(N/128) * BH).  Q, dO and dQ maps
+// d = 64, 128: the 128-wide variants (fa_bwd_wide.cu), same arguments.
+cudaError_t launch_bwd_dkdv_wide(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                 const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq_wide(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                               const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                               const CUtensorMap& tmdQ, const BwdArgs& a, cudaStream_t stream);
+// dQ: grid = ceil(N/128) * BH.  Q, dO and dQ maps
 // use 128-row boxes, K and V bwd_dq_krows(d)-row boxes.
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
