@@ -312,12 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int qa = 32 * c + e;
-          float v = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -L2[qa]));
-          if (need_mask) {
-            const int qg = q0 + qa;
-            if (!key_ok || qg >= a.N || (a.causal && key > qg)) v = 0.f;
+          p[qa] = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -L2[qa]));
+        }
+        // One branch per chunk; inside, selects only (a branch per element
+        // in the loop above costs more than the exponentials).
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int qg = q0 + 32 * c + e;
+            const bool keep = key_ok & (qg < a.N) & !((a.causal != 0) & (key > qg));
+            p[32 * c + e] = keep ? p[32 * c + e] : 0.f;
           }
-          p[qa] = v;
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = pack_bf16(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
@@ -595,12 +600,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          float v = ex2(fmaf(__uint_as_float(sr[c][e]), a.scale_log2, -L2));
-          if (need_mask) {
-            const int key = key0 + 32 * c + e;
-            if (key >= kv_limit || (a.causal && key > grow)) v = 0.f;
-          }
-          p[32 * c + e] = v;
+          p[32 * c + e] = ex2(fmaf(__uint_as_float(sr[c][e]), a.scale_log2, -L2));
+        }
+      }
+      // One branch per step; inside, selects only.
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int key = key0 + e;
+          const bool keep = (key < kv_limit) & !((a.causal != 0) & (key > grow));
+          p[e] = keep ? p[e] : 0.f;
         }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, j & 1, ab))) {

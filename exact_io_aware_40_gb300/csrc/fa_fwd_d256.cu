@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int key = key0 + 32 * c + e;
-            if (key >= kv_limit || (a.causal && key > grow)) sr[c][e] = __float_as_uint(-INFINITY);
+            const bool keep = (key < kv_limit) & !((a.causal != 0) & (key > grow));
+            sr[c][e] = keep ? sr[c][e] : __float_as_uint(-INFINITY);  // select, no branch
           }
       }
       // Row max as a tree (independent partial maxima, no long dependency chain).
