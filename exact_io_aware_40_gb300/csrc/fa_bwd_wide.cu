@@ -20,9 +20,13 @@
 //   dK_i, dP^T_{i+1} (after dK_i has read dS^T_i).
 // fa_bwd_dq_wide_kernel -- one CTA per 128-row query block, 128-key steps j.
 //   TMEM: two S buffers 0-127 and 128-255 (S_{j+1} is computed while the
-//   warpgroups work on S_j), dP 256-383 (dS over its column halves as above),
-//   dQ 384... Warpgroup A handles key columns 0-63, B 64-127.  Issue order per
-//   step: dQ_j (after dS_j), dP_{j+1}, S_{j+2}.
+//   warpgroups work on S_j), dP 256-383, dQ 384...  Warpgroup A handles key
+//   columns 0-63, B 64-127.  dS_j goes over the first half of each
+//   warpgroup's columns of S_j's buffer (read before), so the dP buffer is
+//   free once the warpgroups have loaded dP_j: dP_{j+1} is issued then, and
+//   the products overlap the warpgroups' work instead of waiting on it.
+//   Issue order per step: dP_{j+1} (after dP_j is read), dQ_j (after dS_j),
+//   S_{j+2} (into S_j's buffer, after dQ_j has read dS_j).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -295,72 +299,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (i_start + it) * kT + 64 * x;  // first query column of this half
       const float* L2 = sLD + lst * 256 + 64 * x;
       const float* Dv = sLD + lst * 256 + 128 + 64 * x;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_ld_full(lst), (it / C::kLdSt) & 1, ab) &&
-                                       mbar_wait(bar_s, it & 1, ab))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool need_mask = !key_ok || (q0 + 64 > a.N) || (a.causal && q0 < k0 + kT - 1);
+      // ---- P^T: on the critical path (S^T -> P^T -> dV -> next S^T)
+      const bool ok1 = ok && __all_sync(0xffffffffu,
+                                        mbar_wait(bar_ld_full(lst), (it / C::kLdSt) & 1, ab) &&
+                                            mbar_wait(bar_s, it & 1, ab));
       float p[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(tl + cs + 32 * c, sr);
+      if (ok1) {
+        tc_fence_after();
+        const bool need_mask = !key_ok || (q0 + 64 > a.N) || (a.causal && q0 < k0 + kT - 1);
+        uint32_t sr[2][32];
+        tmem_ld32(tl + cs, sr[0]);
+        tmem_ld32(tl + cs + 32, sr[1]);
         tmem_wait_ld();
-        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int qa = 32 * c + e;
-          p[qa] = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -L2[qa]));
-        }
-        // One branch per chunk; inside, selects only (a branch per element
-        // in the loop above costs more than the exponentials).
+        for (int e = 0; e < 64; ++e)
+          p[e] = ex2(fmaf(__uint_as_float(sr[e >> 5][e & 31]), a.scale_log2, -L2[e]));
+        // One branch per step; inside, selects only (a branch per element in
+        // the loop above costs more than the exponentials).
         if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qg = q0 + 32 * c + e;
+          for (int e = 0; e < 64; ++e) {
+            const int qg = q0 + e;
             const bool keep = key_ok & (qg < a.N) & !((a.causal != 0) & (key > qg));
-            p[32 * c + e] = keep ? p[32 * c + e] : 0.f;
+            p[e] = keep ? p[e] : 0.f;
           }
         }
+        uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
-        // P^T over columns this thread has read (first half of its S^T columns)
-        tmem_st16(tl + cs + 16 * c, w);
+        for (int e = 0; e < 32; ++e) w[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+        // P^T over the first half of this warpgroup's S^T columns (read above)
+        tmem_st32(tl + cs, w);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
-
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, it & 1, ab))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // Both warpgroups finish P^T before either starts dS^T.  dS^T feeds dK,
+      // which the MMA warp issues only after dV and the next S^T, so it has
+      // slack; P^T has none, and running the two side by side slowed P^T.
+      // Every exit of the loop passes through this barrier, so a warpgroup
+      // that stops early cannot leave the other waiting.
+      ok = bar_and_w(3, 256, ok1);
+      if (!ok) break;
+      // ---- dS^T
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, it & 1, ab));
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dr[32];
-        tmem_ld32(tl + cdp + 32 * c, dr);
-        tmem_wait_ld();
-        uint32_t w[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dr[32];
+          tmem_ld32(tl + cdp + 32 * c, dr);
+          tmem_wait_ld();
+          uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int qa = 32 * c + 2 * e;
-          const float d0 = p[qa] * (__uint_as_float(dr[2 * e]) - Dv[qa]);
-          const float d1 = p[qa + 1] * (__uint_as_float(dr[2 * e + 1]) - Dv[qa + 1]);
-          w[e] = pack_bf16(d0, d1);
+          for (int e = 0; e < 16; ++e) {
+            const int qa = 32 * c + 2 * e;
+            const float d0 = p[qa] * (__uint_as_float(dr[2 * e]) - Dv[qa]);
+            const float d1 = p[qa + 1] * (__uint_as_float(dr[2 * e + 1]) - Dv[qa + 1]);
+            w[e] = pack_bf16(d0, d1);
+          }
+          tmem_st16(tl + cdp + 16 * c, w);  // dS^T over columns this thread has read
         }
-        tmem_st16(tl + cdp + 16 * c, w);  // dS^T over columns this thread has read
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_ds);
+          mbar_arrive(bar_ld_empty(lst));  // this step's L, D have been read
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_ds);
-        mbar_arrive(bar_ld_empty(lst));  // this step's L, D have been read
-      }
+      // A failed wait here reaches the barrier above in the next step (its
+      // waits fail at once) or ends the loop.
     }
     if (ok && n_iter > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_final, 0, ab));
@@ -412,13 +421,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD>
 struct QW {
   using W = WCfg<HD>;
+  // Separate K and V rings.  V_j is free once dP_j has completed, K_j only
+  // after dQ_j; K_{j+2} must arrive before S_{j+2}, which is issued right
+  // after dQ_j, so K needs one stage more than V.
+  static constexpr int kKSt = HD == 64 ? 4 : 3;
+  static constexpr int kVSt = HD == 64 ? 3 : 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffdO = W::kTile;
-  static constexpr int kOffK = 2 * W::kTile;                 // kSt stages
-  static constexpr int kOffV = kOffK + W::kSt * W::kTile;    // kSt stages
-  static constexpr int kOffBar = kOffV + W::kSt * W::kTile;
-  // q_full, kv_full[], kv_empty[], s[2], dp, ds, final, drain
-  static constexpr int kNumBar = 1 + 2 * W::kSt + 6;
+  static constexpr int kOffK = 2 * W::kTile;
+  static constexpr int kOffV = kOffK + kKSt * W::kTile;
+  static constexpr int kOffBar = kOffV + kVSt * W::kTile;
+  // q_full, k_full[], k_empty[], v_full[], v_empty[], s[2], dp, ds, final, drain, dp_free
+  static constexpr int kNumBar = 1 + 2 * kKSt + 2 * kVSt + 7;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -443,11 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = sb + C::kOffQ, sdO = sb + C::kOffdO, sK = sb + C::kOffK, sV = sb + C::kOffV;
   const uint32_t bar0 = sb + C::kOffBar;
   const uint32_t bar_q = bar0;
-  auto bar_kvfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kvempty = [&](int s) { return bar0 + 8u * (1 + W::kSt + s); };
-  const uint32_t barx = bar0 + 8u * (1 + 2 * W::kSt);
+  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_kempty = [&](int s) { return bar0 + 8u * (1 + C::kKSt + s); };
+  auto bar_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * C::kKSt + s); };
+  auto bar_vempty = [&](int s) { return bar0 + 8u * (1 + 2 * C::kKSt + C::kVSt + s); };
+  const uint32_t barx = bar0 + 8u * (1 + 2 * C::kKSt + 2 * C::kVSt);
   auto bar_s = [&](int b2) { return barx + 8u * b2; };
   const uint32_t bar_dp = barx + 16, bar_ds = barx + 24, bar_final = barx + 32, bar_drain = barx + 40;
+  const uint32_t bar_dpfree = barx + 48;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -464,9 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < W::kSt; ++s) {
-      mbar_init(bar_kvfull(s), 1);
-      mbar_init(bar_kvempty(s), 1);
+    for (int s = 0; s < C::kKSt; ++s) {
+      mbar_init(bar_kfull(s), 1);
+      mbar_init(bar_kempty(s), 1);
+    }
+    for (int s = 0; s < C::kVSt; ++s) {
+      mbar_init(bar_vfull(s), 1);
+      mbar_init(bar_vempty(s), 1);
     }
     mbar_init(bar_s(0), 1);
     mbar_init(bar_s(1), 1);
@@ -474,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_ds, 8);
     mbar_init(bar_final, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_dpfree, 8);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -502,24 +524,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ + c * 16384, &tmQ, c * 64, q0, bh, bar_q, pol_q);
         tma_load_3d(sdO + c * 16384, &tmdO, c * 64, q0, bh, bar_q, pol_q);
       }
-      int last[W::kSt];
-      for (int s = 0; s < W::kSt; ++s) last[s] = -1;
+      int lastk[C::kKSt], lastv[C::kVSt];
+      for (int s = 0; s < C::kKSt; ++s) lastk[s] = -1;
+      for (int s = 0; s < C::kVSt; ++s) lastv[s] = -1;
       for (int j = 0; j < T; ++j) {
-        const int st = j % W::kSt;
-        if (j >= W::kSt && !mbar_wait(bar_kvempty(st), ((j / W::kSt) & 1) ^ 1, ab)) break;
-        mbar_arrive_expect_tx(bar_kvfull(st), 2 * W::kTile);
-        for (int c = 0; c < W::kAtoms; ++c) {
-          tma_load_3d(sK + st * W::kTile + c * 16384, &tmK, c * 64, j * kT, bh, bar_kvfull(st),
+        const int sk = j % C::kKSt, sv = j % C::kVSt;
+        if (j >= C::kKSt && !mbar_wait(bar_kempty(sk), ((j / C::kKSt) & 1) ^ 1, ab)) break;
+        mbar_arrive_expect_tx(bar_kfull(sk), W::kTile);
+        for (int c = 0; c < W::kAtoms; ++c)
+          tma_load_3d(sK + sk * W::kTile + c * 16384, &tmK, c * 64, j * kT, bh, bar_kfull(sk),
                       pol_kv);
-          tma_load_3d(sV + st * W::kTile + c * 16384, &tmV, c * 64, j * kT, bh, bar_kvfull(st),
+        lastk[sk] = j;
+        if (j >= C::kVSt && !mbar_wait(bar_vempty(sv), ((j / C::kVSt) & 1) ^ 1, ab)) break;
+        mbar_arrive_expect_tx(bar_vfull(sv), W::kTile);
+        for (int c = 0; c < W::kAtoms; ++c)
+          tma_load_3d(sV + sv * W::kTile + c * 16384, &tmV, c * 64, j * kT, bh, bar_vfull(sv),
                       pol_kv);
-        }
-        last[st] = j;
+        lastv[sv] = j;
       }
       if (*abort_flag) {
         mbar_wait_drain(bar_q, 0);
-        for (int s = 0; s < W::kSt; ++s)
-          if (last[s] >= 0) mbar_wait_drain(bar_kvfull(s), (last[s] / W::kSt) & 1);
+        for (int s = 0; s < C::kKSt; ++s)
+          if (lastk[s] >= 0) mbar_wait_drain(bar_kfull(s), (lastk[s] / C::kKSt) & 1);
+        for (int s = 0; s < C::kVSt; ++s)
+          if (lastv[s] >= 0) mbar_wait_drain(bar_vfull(s), (lastv[s] / C::kVSt) & 1);
       }
     }
   } else if (warp == 1) {
@@ -529,43 +557,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idQ = idesc_bf16(kT, HD, false, true);   // dQ
       // S_j = Q K_j^T into buffer j & 1
       auto issue_s = [&](int j) -> bool {
-        const int st = j % W::kSt;
-        if (!mbar_wait(bar_kvfull(st), (j / W::kSt) & 1, ab)) return false;
+        const int sk = j % C::kKSt;
+        if (!mbar_wait(bar_kfull(sk), (j / C::kKSt) & 1, ab)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + C::kColS + 128u * (j & 1), kmaj128(sQ, k), kmaj128(sK + st * W::kTile, k),
+          mma_ss(tmem + C::kColS + 128u * (j & 1), kmaj128(sQ, k), kmaj128(sK + sk * W::kTile, k),
                  idS, k > 0 ? 1u : 0u);
         mma_commit(bar_s(j & 1));
         return true;
       };
-      // dP_j = dO V_j^T (its stage was waited for by issue_s(j))
-      auto issue_dp = [&](int j) {
-        const int st = j % W::kSt;
+      // dP_j = dO V_j^T; V_j's stage is free again once it completes.
+      auto issue_dp = [&](int j) -> bool {
+        const int sv = j % C::kVSt;
+        if (!mbar_wait(bar_vfull(sv), (j / C::kVSt) & 1, ab)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + C::kColdP, kmaj128(sdO, k), kmaj128(sV + st * W::kTile, k), idS,
+          mma_ss(tmem + C::kColdP, kmaj128(sdO, k), kmaj128(sV + sv * W::kTile, k), idS,
                  k > 0 ? 1u : 0u);
         mma_commit(bar_dp);
+        mma_commit(bar_vempty(sv));
+        return true;
       };
       bool ok = mbar_wait(bar_q, 0, ab);
       if (ok) ok = issue_s(0);
-      if (ok) issue_dp(0);
+      if (ok) ok = issue_dp(0);
       if (ok && T > 1) ok = issue_s(1);
       for (int j = 0; ok && j < T; ++j) {
-        const int st = j % W::kSt;
+        const int sk = j % C::kKSt;
+        // dP_{j+1} as soon as the warpgroups hold dP_j in registers.
+        if (j + 1 < T) {
+          if (!(ok = mbar_wait(bar_dpfree, j & 1, ab))) break;
+          tc_fence_after();
+          if (!(ok = issue_dp(j + 1))) break;
+        }
         if (!(ok = mbar_wait(bar_ds, j & 1, ab))) break;
         tc_fence_after();
-        // dQ += dS K_j (dS halves at columns 256 and 320; B = K_j MN-major)
+        // dQ += dS_j K_j (dS_j halves at columns 0 and 64 of S_j's buffer;
+        // B = K_j MN-major)
+        const uint32_t sb = C::kColS + 128u * (j & 1);
 #pragma unroll
         for (int k = 0; k < kT / 16; ++k)
-          mma_ts(tmem + C::kColdQ, tmem + split_col(C::kColdP, C::kColdP + 64, k),
-                 mnmaj128(sK + st * W::kTile, k), idQ, (j > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColdQ, tmem + split_col(sb, sb + 64, k),
+                 mnmaj128(sK + sk * W::kTile, k), idQ, (j > 0 || k > 0) ? 1u : 0u);
         if (j == T - 1) mma_commit(bar_final);
-        mma_commit(bar_kvempty(st));
-        // dP_{j+1} overwrites dS_j (read by the product above: in-order);
-        // S_{j+2} takes the buffer of S_j, which the warpgroups have read.
-        if (j + 1 < T) issue_dp(j + 1);
+        mma_commit(bar_kempty(sk));
+        // S_{j+2} overwrites dS_j: the product above reads it first (in order).
         if (j + 2 < T && !(ok = issue_s(j + 2))) break;
       }
       mma_commit(bar_drain);
@@ -617,20 +655,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      uint32_t dr[2][32];
+      tmem_ld32(tl + cdp, dr[0]);
+      tmem_ld32(tl + cdp + 32, dr[1]);
+      tmem_wait_ld();
+      // dP_j is in registers: the MMA warp may overwrite the dP buffer.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dpfree);
+      uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dr[32];
-        tmem_ld32(tl + cdp + 32 * c, dr);
-        tmem_wait_ld();
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float d0 = p[32 * c + 2 * e] * (__uint_as_float(dr[2 * e]) - Dr);
-          const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - Dr);
-          w[e] = pack_bf16(d0, d1);
-        }
-        tmem_st16(tl + cdp + 16 * c, w);  // dS over columns this thread has read
+      for (int e = 0; e < 32; ++e) {
+        const float d0 = p[2 * e] * (__uint_as_float(dr[e >> 4][(2 * e) & 31]) - Dr);
+        const float d1 = p[2 * e + 1] * (__uint_as_float(dr[e >> 4][(2 * e + 1) & 31]) - Dr);
+        w[e] = pack_bf16(d0, d1);
       }
+      // dS over the first half of this warpgroup's columns of S_j's buffer
+      tmem_st32(tl + C::kColS + 128u * (j & 1) + 64u * x, w);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
