@@ -20,7 +20,9 @@
  *
  *   For one (batch b, head h), with rows q_i, k_j, v_j of Q, K, V (d wide):
  *     s_ij = scale * sum_c q_ic k_jc
- *     M(i) = { j : j < len_b  and (not causal or j <= i) }   (visible keys)
+ *     M(i) = { j : j < len_b  and (not causal or j <= i)
+ *                 and (w < 0 or i - w <= j <= i)
+ *                 and (no block mask or bm[i / bs][j / bs] != 0) }   (visible keys)
  *     m_i  = max_{j in M(i)} s_ij
  *     p_ij = exp(s_ij - m_i) / sum_{j' in M(i)} exp(s_ij' - m_i),  j in M(i)
  *     p_ij = 0                                                   otherwise
@@ -38,6 +40,14 @@
  *     dQ   = scale * dS K
  *     dK   = scale * dS^T Q
  *
+ * The two optional mask terms are the pages' extensions: a sliding (local)
+ * window, named as a feature in the bxzpzcl.cn article (section "高级功能配置"),
+ * read as the causal band of the w keys before each query plus the query's
+ * own position; and block-sparse attention (the paper's abstract; fmread.com
+ * summary, section 六 item 3), read as a 0/1 mask over (query block, key
+ * block) pairs of bs x bs positions: pairs with 0 are left out, every other
+ * mask still applies inside the pairs kept.
+ *
  * Memory: S and P are materialised for a panel of complete rows (all keys of
  * each row), so every softmax is a plain two-pass safe softmax: no online
  * rescaling appears here.  Tensors are contiguous [B, H, N, d] fp64; L and
@@ -53,10 +63,36 @@
 #define ORACLE_ERR_ARG 1
 #define ORACLE_ERR_NOMEM 2
 
+/* The mask terms of one (batch, head). */
+typedef struct {
+    int causal;
+    int64_t len;                 /* len_b */
+    int64_t window;              /* w; < 0: no window */
+    const unsigned char *bmask;  /* [ceil(N/bs)][ceil(N/bs)] or NULL */
+    int64_t bs, nkb;             /* block size, key blocks per mask row */
+} mask_t;
+
 /* Is key j visible from query i? (the mask set M(i) above) */
-static int visible(int64_t i, int64_t j, int causal, int64_t len)
+static int visible(int64_t i, int64_t j, const mask_t *m)
 {
-    return j < len && (!causal || j <= i);
+    if (j >= m->len) return 0;
+    if (m->causal && j > i) return 0;
+    if (m->window >= 0 && (j > i || j < i - m->window)) return 0;
+    if (m->bmask && !m->bmask[(i / m->bs) * m->nkb + j / m->bs]) return 0;
+    return 1;
+}
+
+static mask_t make_mask(int causal, int64_t len, int window, const unsigned char *bmask,
+                        int bs, int64_t N)
+{
+    mask_t m;
+    m.causal = causal;
+    m.len = len;
+    m.window = window;
+    m.bmask = bmask;
+    m.bs = bs > 0 ? bs : 1;
+    m.nkb = (N + m.bs - 1) / m.bs;
+    return m;
 }
 
 static double dot(const double *a, const double *b, int d)
@@ -129,7 +165,7 @@ static void run_pool(task_fn fn, void *ctx, int64_t ntasks, int nthreads)
  * lse[r] = the row's logsumexp.  Entries outside M(i) get p = 0 (s is left at
  * 0 there and never read). */
 static void panel_probs(const double *q, const double *k, int64_t N, int d,
-                        double scale, int causal, int64_t len, int64_t r0,
+                        double scale, const mask_t *msk, int64_t r0,
                         int64_t R, double *s, double *p, double *lse)
 {
     for (int64_t r = 0; r < R; ++r) {
@@ -138,7 +174,7 @@ static void panel_probs(const double *q, const double *k, int64_t N, int d,
         double *prow = p + r * N;
         double mx = -INFINITY;
         for (int64_t j = 0; j < N; ++j) {
-            if (visible(i, j, causal, len)) {
+            if (visible(i, j, msk)) {
                 srow[j] = scale * dot(q + i * d, k + j * d, d);
                 if (srow[j] > mx) mx = srow[j];
             } else {
@@ -152,7 +188,7 @@ static void panel_probs(const double *q, const double *k, int64_t N, int d,
         }
         double sum = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            if (visible(i, j, causal, len)) {
+            if (visible(i, j, msk)) {
                 prow[j] = exp(srow[j] - mx);
                 sum += prow[j];
             } else {
@@ -183,6 +219,9 @@ typedef struct {
     double scale;
     int causal;
     const int *kv_len;
+    int window;
+    const unsigned char *bmask;
+    int bs;
     double *o, *L;
     int err;
 } fwd_ctx_t;
@@ -195,6 +234,7 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
     int d = c->d;
     int64_t b = bh / c->H;
     int64_t len = c->kv_len ? c->kv_len[b] : N;
+    mask_t msk = make_mask(c->causal, len, c->window, c->bmask, c->bs, N);
     const double *q = c->q + bh * N * d, *k = c->k + bh * N * d, *v = c->v + bh * N * d;
     double *o = c->o + bh * N * d, *L = c->L + bh * N;
     int64_t R = panel_rows(N);
@@ -208,7 +248,7 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
     }
     for (int64_t r0 = 0; r0 < N; r0 += R) {
         int64_t rr = (r0 + R <= N) ? R : N - r0;
-        panel_probs(q, k, N, d, c->scale, c->causal, len, r0, rr, s, p, lse);
+        panel_probs(q, k, N, d, c->scale, &msk, r0, rr, s, p, lse);
         for (int64_t r = 0; r < rr; ++r) {
             int64_t i = r0 + r;
             double *oi = o + i * d;
@@ -226,11 +266,14 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
 }
 
 int oracle_attn_fwd(const double *q, const double *k, const double *v, int B, int H,
-                    int N, int d, double scale, int causal, const int *kv_len,
-                    double *o, double *L, int nthreads)
+                    int N, int d, double scale, int causal, const int *kv_len, int window,
+                    const unsigned char *block_mask, int block, double *o, double *L,
+                    int nthreads)
 {
     if (!q || !k || !v || !o || !L || B < 0 || H < 0 || N < 0 || d < 1) return ORACLE_ERR_ARG;
-    fwd_ctx_t c = {q, k, v, H, N, d, scale, causal, kv_len, o, L, ORACLE_OK};
+    if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    fwd_ctx_t c = {q, k, v, H, N, d, scale, causal, kv_len, window, block_mask, block,
+                   o, L, ORACLE_OK};
     run_pool(fwd_task, &c, (int64_t)B * H, nthreads);
     return c.err;
 }
@@ -245,6 +288,9 @@ typedef struct {
     double scale;
     int causal;
     const int *kv_len;
+    int window;
+    const unsigned char *bmask;
+    int bs;
     double *dq, *dk, *dv;
     int err;
 } bwd_ctx_t;
@@ -257,6 +303,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
     int d = c->d;
     int64_t b = bh / c->H;
     int64_t len = c->kv_len ? c->kv_len[b] : N;
+    mask_t msk = make_mask(c->causal, len, c->window, c->bmask, c->bs, N);
     int64_t off = bh * N * d;
     const double *q = c->q + off, *k = c->k + off, *v = c->v + off, *dout = c->dout + off;
     double *dq = c->dq + off, *dk = c->dk + off, *dv = c->dv + off;
@@ -274,7 +321,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
     memset(dv, 0, sizeof(double) * (size_t)(N * d));
     for (int64_t r0 = 0; r0 < N; r0 += R) {
         int64_t rr = (r0 + R <= N) ? R : N - r0;
-        panel_probs(q, k, N, d, c->scale, c->causal, len, r0, rr, s, p, lse);
+        panel_probs(q, k, N, d, c->scale, &msk, r0, rr, s, p, lse);
         for (int64_t r = 0; r < rr; ++r) {
             int64_t i = r0 + r;
             const double *doi = dout + i * d;
@@ -282,7 +329,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
             /* dP_ij = dO_i . v_j and D_i = sum_j p_ij dP_ij */
             double Di = 0.0;
             for (int64_t j = 0; j < N; ++j) {
-                dprow[j] = visible(i, j, c->causal, len) ? dot(doi, v + j * d, d) : 0.0;
+                dprow[j] = visible(i, j, &msk) ? dot(doi, v + j * d, d) : 0.0;
                 Di += prow[j] * dprow[j];
             }
             double *dqi = dq + i * d;
@@ -307,11 +354,14 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
 
 int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
                     int B, int H, int N, int d, double scale, int causal, const int *kv_len,
+                    int window, const unsigned char *block_mask, int block,
                     double *dq, double *dk, double *dv, int nthreads)
 {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H < 0 || N < 0 || d < 1)
         return ORACLE_ERR_ARG;
-    bwd_ctx_t c = {q, k, v, dout, H, N, d, scale, causal, kv_len, dq, dk, dv, ORACLE_OK};
+    if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    bwd_ctx_t c = {q, k, v, dout, H, N, d, scale, causal, kv_len, window, block_mask, block,
+                   dq, dk, dv, ORACLE_OK};
     run_pool(bwd_task, &c, (int64_t)B * H, nthreads);
     return c.err;
 }
@@ -323,10 +373,13 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
 
 /* o_out[r*d..], L_out[r] for the listed query rows. */
 int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, int d,
-                    double scale, int causal, int len, int nrows, const int *rows,
+                    double scale, int causal, int len, int window,
+                    const unsigned char *block_mask, int block, int nrows, const int *rows,
                     double *o_out, double *L_out)
 {
     if (!q || !k || !v || !rows || !o_out || !L_out || N < 1 || d < 1) return ORACLE_ERR_ARG;
+    if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    mask_t msk = make_mask(causal, len, window, block_mask, block, N);
     double *s = (double *)malloc(sizeof(double) * (size_t)N);
     double *p = (double *)malloc(sizeof(double) * (size_t)N);
     if (!s || !p) { free(s); free(p); return ORACLE_ERR_NOMEM; }
@@ -334,7 +387,7 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, in
         int64_t i = rows[r];
         if (i < 0 || i >= N) { free(s); free(p); return ORACLE_ERR_ARG; }
         double lse;
-        panel_probs(q, k, N, d, scale, causal, len, i, 1, s, p, &lse);
+        panel_probs(q, k, N, d, scale, &msk, i, 1, s, p, &lse);
         for (int c = 0; c < d; ++c) o_out[(int64_t)r * d + c] = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             if (p[j] == 0.0) continue;
@@ -349,10 +402,13 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, in
 /* dq_out[r*d..] for the listed query rows (each dQ row needs only its own
  * row of P and dP). */
 int oracle_bwd_dq_rows(const double *q, const double *k, const double *v, const double *dout,
-                       int N, int d, double scale, int causal, int len, int nrows,
+                       int N, int d, double scale, int causal, int len, int window,
+                       const unsigned char *block_mask, int block, int nrows,
                        const int *rows, double *dq_out)
 {
     if (!q || !k || !v || !dout || !rows || !dq_out || N < 1 || d < 1) return ORACLE_ERR_ARG;
+    if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    mask_t msk = make_mask(causal, len, window, block_mask, block, N);
     double *s = (double *)malloc(sizeof(double) * (size_t)N);
     double *p = (double *)malloc(sizeof(double) * (size_t)N);
     double *dp = (double *)malloc(sizeof(double) * (size_t)N);
@@ -361,11 +417,11 @@ int oracle_bwd_dq_rows(const double *q, const double *k, const double *v, const 
         int64_t i = rows[r];
         if (i < 0 || i >= N) { free(s); free(p); free(dp); return ORACLE_ERR_ARG; }
         double lse;
-        panel_probs(q, k, N, d, scale, causal, len, i, 1, s, p, &lse);
+        panel_probs(q, k, N, d, scale, &msk, i, 1, s, p, &lse);
         const double *doi = dout + i * d;
         double Di = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            dp[j] = visible(i, j, causal, len) ? dot(doi, v + j * d, d) : 0.0;
+            dp[j] = visible(i, j, &msk) ? dot(doi, v + j * d, d) : 0.0;
             Di += p[j] * dp[j];
         }
         double *dqi = dq_out + (int64_t)r * d;
@@ -387,8 +443,7 @@ typedef struct {
     int64_t N;
     int d;
     double scale;
-    int causal;
-    int64_t len;
+    const mask_t *msk;
     double *lse, *D;
 } rowstat_ctx_t;
 
@@ -402,7 +457,7 @@ static void rowstat_task(void *vctx, int64_t i, int worker)
     double *p = (double *)malloc(sizeof(double) * (size_t)N);
     if (!s || !p) { free(s); free(p); c->lse[i] = NAN; return; }
     double lse;
-    panel_probs(c->q, c->k, N, d, c->scale, c->causal, c->len, i, 1, s, p, &lse);
+    panel_probs(c->q, c->k, N, d, c->scale, c->msk, i, 1, s, p, &lse);
     double Di = 0.0;
     for (int64_t j = 0; j < N; ++j)
         if (p[j] != 0.0) Di += p[j] * dot(c->dout + i * d, c->v + j * d, d);
@@ -413,15 +468,18 @@ static void rowstat_task(void *vctx, int64_t i, int worker)
 
 int oracle_bwd_dkdv_cols(const double *q, const double *k, const double *v,
                          const double *dout, int N, int d, double scale, int causal,
-                         int len, int ncols, const int *cols, double *dk_out,
+                         int len, int window, const unsigned char *block_mask, int block,
+                         int ncols, const int *cols, double *dk_out,
                          double *dv_out, int nthreads)
 {
     if (!q || !k || !v || !dout || !cols || !dk_out || !dv_out || N < 1 || d < 1)
         return ORACLE_ERR_ARG;
+    if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    mask_t msk = make_mask(causal, len, window, block_mask, block, N);
     double *lse = (double *)malloc(sizeof(double) * (size_t)N);
     double *D = (double *)malloc(sizeof(double) * (size_t)N);
     if (!lse || !D) { free(lse); free(D); return ORACLE_ERR_NOMEM; }
-    rowstat_ctx_t rc = {q, k, v, dout, N, d, scale, causal, len, lse, D};
+    rowstat_ctx_t rc = {q, k, v, dout, N, d, scale, &msk, lse, D};
     run_pool(rowstat_task, &rc, N, nthreads);
     for (int64_t i = 0; i < N; ++i)
         if (isnan(lse[i])) { free(lse); free(D); return ORACLE_ERR_NOMEM; }
@@ -431,7 +489,7 @@ int oracle_bwd_dkdv_cols(const double *q, const double *k, const double *v,
         double *dkj = dk_out + (int64_t)r * d, *dvj = dv_out + (int64_t)r * d;
         for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
         for (int64_t i = 0; i < N; ++i) {
-            if (!visible(i, j, causal, len)) continue;
+            if (!visible(i, j, &msk)) continue;
             double pij = exp(scale * dot(q + i * d, k + j * d, d) - lse[i]);
             double dpij = dot(dout + i * d, v + j * d, d);
             double ds = pij * (dpij - D[i]);

@@ -7,6 +7,11 @@ check and the benchmark's CPU-baseline leg may use it.
 
 Inputs are numpy float64 arrays, contiguous ``[B, H, N, d]``; bf16 inputs are
 widened exactly by the caller before they reach this module.
+
+Mask arguments shared by every function: ``causal``; ``kv_len`` (or the
+per-head ``length``); ``window`` (``w >= 0`` keeps only keys ``i - w <= j <=
+i``; ``-1`` for none); ``block_mask`` (uint8 ``[ceil(N/block), ceil(N/block)]``
+over (query block, key block) pairs, 0 = left out; ``None`` for none).
 """
 import ctypes
 import os
@@ -45,11 +50,14 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         i, d = ctypes.c_int, ctypes.c_double
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, i, i, i, i, d, i, ip, dp, dp, i]
-        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, d, i, ip, dp, dp, dp, i]
-        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, i, i, d, i, i, i, ip, dp, dp]
-        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, ip, dp]
-        lib.oracle_bwd_dkdv_cols.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, ip, dp, dp, i]
+        bp = ctypes.POINTER(ctypes.c_ubyte)
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, i, i, i, i, d, i, ip, i, bp, i, dp, dp, i]
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, d, i, ip, i, bp, i,
+                                        dp, dp, dp, i]
+        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, i, i, d, i, i, i, bp, i, i, ip, dp, dp]
+        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, bp, i, i, ip, dp]
+        lib.oracle_bwd_dkdv_cols.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, bp, i, i, ip,
+                                             dp, dp, i]
         for f in ("oracle_attn_fwd", "oracle_attn_bwd", "oracle_fwd_rows",
                   "oracle_bwd_dq_rows", "oracle_bwd_dkdv_cols"):
             getattr(lib, f).restype = ctypes.c_int
@@ -67,12 +75,24 @@ def _i32(a):
     return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
 
 
+def _mask(block_mask, N, block):
+    """(keep-alive array, pointer) of a block mask, checked against N."""
+    if block_mask is None:
+        return None, None
+    nb = (N + block - 1) // block
+    m = np.ascontiguousarray(block_mask, dtype=np.uint8)
+    if m.shape != (nb, nb):
+        raise ValueError("block_mask must be [%d, %d] for N=%d, block=%d" % (nb, nb, N, block))
+    return m, m.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+
+
 def _check(rc, name):
     if rc != 0:
         raise RuntimeError("oracle %s failed with code %d" % (name, rc))
 
 
-def attn_fwd(q, k, v, scale, causal=False, kv_len=None, nthreads=None):
+def attn_fwd(q, k, v, scale, causal=False, kv_len=None, nthreads=None, window=-1,
+             block_mask=None, block=128):
     """Standard attention forward.  Returns (O [B,H,N,d], L [B,H,N]) in fp64."""
     lib = _load()
     B, H, N, d = q.shape
@@ -85,13 +105,16 @@ def attn_fwd(q, k, v, scale, causal=False, kv_len=None, nthreads=None):
         kv, kvp = _i32(kv_len)
     else:
         kv, kvp = None, None
+    bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_attn_fwd(qp, kp, vp, B, H, N, d, float(scale), int(bool(causal)), kvp,
+                             int(window), bmp, int(block),
                              _f64(o)[1], _f64(L)[1], int(nthreads or default_threads()))
     _check(rc, "attn_fwd")
     return o, L
 
 
-def attn_bwd(q, k, v, dout, scale, causal=False, kv_len=None, nthreads=None):
+def attn_bwd(q, k, v, dout, scale, causal=False, kv_len=None, nthreads=None, window=-1,
+             block_mask=None, block=128):
     """Gradients of standard attention.  Returns (dQ, dK, dV), fp64 [B,H,N,d]."""
     lib = _load()
     B, H, N, d = q.shape
@@ -106,14 +129,16 @@ def attn_bwd(q, k, v, dout, scale, causal=False, kv_len=None, nthreads=None):
         kv, kvp = _i32(kv_len)
     else:
         kv, kvp = None, None
+    bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_attn_bwd(qp, kp, vp, dop, B, H, N, d, float(scale), int(bool(causal)), kvp,
+                             int(window), bmp, int(block),
                              _f64(dq)[1], _f64(dk)[1], _f64(dv)[1],
                              int(nthreads or default_threads()))
     _check(rc, "attn_bwd")
     return dq, dk, dv
 
 
-def fwd_rows(q, k, v, scale, causal, length, rows):
+def fwd_rows(q, k, v, scale, causal, length, rows, window=-1, block_mask=None, block=128):
     """O and L rows of ONE head (q, k, v are [N, d]) at the listed query rows."""
     lib = _load()
     N, d = q.shape
@@ -123,13 +148,15 @@ def fwd_rows(q, k, v, scale, causal, length, rows):
     rows, rp = _i32(rows)
     o = np.empty((len(rows), d), np.float64)
     L = np.empty((len(rows),), np.float64)
+    bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_fwd_rows(qp, kp, vp, N, d, float(scale), int(bool(causal)), int(length),
-                             len(rows), rp, _f64(o)[1], _f64(L)[1])
+                             int(window), bmp, int(block), len(rows), rp, _f64(o)[1], _f64(L)[1])
     _check(rc, "fwd_rows")
     return o, L
 
 
-def bwd_dq_rows(q, k, v, dout, scale, causal, length, rows):
+def bwd_dq_rows(q, k, v, dout, scale, causal, length, rows, window=-1, block_mask=None,
+                block=128):
     """dQ rows of ONE head at the listed query rows."""
     lib = _load()
     N, d = q.shape
@@ -139,13 +166,16 @@ def bwd_dq_rows(q, k, v, dout, scale, causal, length, rows):
     dout, dop = _f64(dout)
     rows, rp = _i32(rows)
     dq = np.empty((len(rows), d), np.float64)
+    bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_bwd_dq_rows(qp, kp, vp, dop, N, d, float(scale), int(bool(causal)),
-                                int(length), len(rows), rp, _f64(dq)[1])
+                                int(length), int(window), bmp, int(block), len(rows), rp,
+                                _f64(dq)[1])
     _check(rc, "bwd_dq_rows")
     return dq
 
 
-def bwd_dkdv_cols(q, k, v, dout, scale, causal, length, cols, nthreads=None):
+def bwd_dkdv_cols(q, k, v, dout, scale, causal, length, cols, nthreads=None, window=-1,
+                  block_mask=None, block=128):
     """dK and dV rows of ONE head at the listed key indices."""
     lib = _load()
     N, d = q.shape
@@ -156,8 +186,10 @@ def bwd_dkdv_cols(q, k, v, dout, scale, causal, length, cols, nthreads=None):
     cols, cp = _i32(cols)
     dk = np.empty((len(cols), d), np.float64)
     dv = np.empty((len(cols), d), np.float64)
+    bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_bwd_dkdv_cols(qp, kp, vp, dop, N, d, float(scale), int(bool(causal)),
-                                  int(length), len(cols), cp, _f64(dk)[1], _f64(dv)[1],
+                                  int(length), int(window), bmp, int(block), len(cols), cp,
+                                  _f64(dk)[1], _f64(dv)[1],
                                   int(nthreads or default_threads()))
     _check(rc, "bwd_dkdv_cols")
     return dk, dv

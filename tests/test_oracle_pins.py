@@ -309,3 +309,157 @@ def test_sampled_rows_and_columns_match_whole_tensor_results(causal, length):
     dk_c, dv_c = oracle.bwd_dkdv_cols(q[0, 0], k[0, 0], v[0, 0], do[0, 0], 0.5, causal, length, cols)
     np.testing.assert_allclose(dk_c, dk[0, 0, cols], atol=1e-13)
     np.testing.assert_allclose(dv_c, dv[0, 0, cols], atol=1e-13)
+
+
+# --- sliding window and block-sparse mask terms --------------------------------
+
+def band_mask(N, window):
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    return (j <= i) & (j >= i - window)
+
+
+def block_to_pos(bm, N, bs):
+    """Expand a (query block, key block) mask to positions."""
+    blk = np.arange(N) // bs
+    return bm[blk[:, None], blk[None, :]].astype(bool)
+
+
+def test_window_zero_attends_to_own_position_only():
+    # With w = 0 every row keeps exactly one key (itself): P is the identity,
+    # so O = V, L = scale q_i.k_i, dV = dO and dS = 0 (dQ = dK = 0).
+    B, H, N, d = 1, 2, 9, 5
+    q, k, v, do = (rand(B, H, N, d) for _ in range(4))
+    o, L = oracle.attn_fwd(q, k, v, 0.7, False, window=0)
+    np.testing.assert_allclose(o, v, atol=1e-14)
+    np.testing.assert_allclose(L, 0.7 * np.einsum("bhic,bhic->bhi", q, k), atol=1e-13)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.7, False, window=0)
+    np.testing.assert_allclose(dv, do, atol=1e-14)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-14)
+
+
+def test_window_rows_ignore_keys_outside_the_band():
+    # Perturbing K, V outside row i's band [i - w, i] leaves row i unchanged.
+    N, d, w = 12, 4, 3
+    q, k, v = (rand(1, 1, N, d) for _ in range(3))
+    o, L = oracle.attn_fwd(q, k, v, 0.5, False, window=w)
+    i = 7
+    k2, v2 = k.copy(), v.copy()
+    outside = [j for j in range(N) if not (i - w <= j <= i)]
+    k2[0, 0, outside] += rand(len(outside), d)
+    v2[0, 0, outside] += rand(len(outside), d)
+    o2, L2 = oracle.attn_fwd(q, k2, v2, 0.5, False, window=w)
+    np.testing.assert_allclose(o2[0, 0, i], o[0, 0, i], atol=1e-14)
+    np.testing.assert_allclose(L2[0, 0, i], L[0, 0, i], atol=1e-14)
+
+
+def test_block_diagonal_mask_equals_independent_blocks():
+    # A block mask that keeps only the diagonal pairs splits the sequence into
+    # independent attention problems, one per block: each must equal the
+    # unmasked oracle run on that block alone.
+    N, d, bs = 11, 6, 4
+    q, k, v, do = (rand(1, 2, N, d) for _ in range(4))
+    nb = (N + bs - 1) // bs
+    bm = np.eye(nb, dtype=np.uint8)
+    o, L = oracle.attn_fwd(q, k, v, 0.4, False, block_mask=bm, block=bs)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.4, False, block_mask=bm, block=bs)
+    for t in range(nb):
+        sl = slice(t * bs, min(N, (t + 1) * bs))
+        ob, Lb = oracle.attn_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], 0.4, False)
+        gq, gk, gv = oracle.attn_bwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], do[:, :, sl], 0.4, False)
+        np.testing.assert_allclose(o[:, :, sl], ob, atol=1e-14)
+        np.testing.assert_allclose(L[:, :, sl], Lb, atol=1e-14)
+        np.testing.assert_allclose(dq[:, :, sl], gq, atol=1e-13)
+        np.testing.assert_allclose(dk[:, :, sl], gk, atol=1e-13)
+        np.testing.assert_allclose(dv[:, :, sl], gv, atol=1e-13)
+
+
+def test_all_ones_block_mask_changes_nothing_and_empty_block_rows_are_zero():
+    N, d, bs = 10, 4, 4
+    q, k, v, do = (rand(1, 1, N, d) for _ in range(4))
+    nb = 3
+    o0, L0 = oracle.attn_fwd(q, k, v, 0.5, True)
+    o1, L1 = oracle.attn_fwd(q, k, v, 0.5, True, block_mask=np.ones((nb, nb), np.uint8), block=bs)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(L0, L1)
+    # query block 1 keeps no key block: its rows are empty (O = 0, L = -inf,
+    # zero gradients), and keys are only reached from the other blocks
+    bm = np.ones((nb, nb), np.uint8)
+    bm[1, :] = 0
+    o, L = oracle.attn_fwd(q, k, v, 0.5, False, block_mask=bm, block=bs)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.5, False, block_mask=bm, block=bs)
+    np.testing.assert_array_equal(o[0, 0, 4:8], 0.0)
+    assert np.all(np.isneginf(L[0, 0, 4:8]))
+    np.testing.assert_array_equal(dq[0, 0, 4:8], 0.0)
+
+
+@pytest.mark.parametrize("causal,window,use_bm", [(False, 2, False), (True, 5, True),
+                                                  (False, -1, True), (True, -1, True)])
+def test_window_and_block_mask_match_torch_fp64_sdpa(causal, window, use_bm):
+    torch = pytest.importorskip("torch")
+    B, H, N, d, bs = 2, 2, 14, 8, 4
+    lens = np.array([14, 10])
+    nb = (N + bs - 1) // bs
+    bm = (np.random.default_rng(7).random((nb, nb)) < 0.6).astype(np.uint8)
+    np.fill_diagonal(bm, 1)   # every query keeps its own position: no empty rows
+    bm_arg = bm if use_bm else None
+    q, k, v, do = (rand(B, H, N, d) for _ in range(4))
+    o, L = oracle.attn_fwd(q, k, v, 0.3, causal, kv_len=lens, window=window,
+                           block_mask=bm_arg, block=bs)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.3, causal, kv_len=lens, window=window,
+                                 block_mask=bm_arg, block=bs)
+    mask = np.zeros((B, 1, N, N), bool)
+    for b in range(B):
+        m = visible_mask(N, causal, lens[b])
+        if window >= 0:
+            m = m & band_mask(N, window)
+        if use_bm:
+            m = m & block_to_pos(bm, N, bs)
+        mask[b, 0] = m
+    # Rows that keep no key (a query block whose kept pairs all lie past
+    # kv_len) are NaN in the library; compare the others, and check the empty
+    # ones against the empty-row convention (O = 0, L = -inf, no gradient).
+    keep = np.broadcast_to(mask.any(-1), (B, H, N))
+    kp = np.broadcast_to(keep[..., None], o.shape)
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.tensor(mask),
+                                                          scale=0.3)
+    to = torch.where(torch.tensor(kp), to, torch.zeros_like(to))
+    to.backward(torch.tensor(np.where(kp, do, 0.0)))
+    np.testing.assert_allclose(o[kp], to.detach().numpy()[kp], atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+    assert np.all(o[~kp] == 0.0) and np.all(np.isneginf(L[~keep])) and np.all(dq[~kp] == 0.0)
+    s = 0.3 * np.einsum("bhic,bhjc->bhij", q, k)
+    s = np.where(mask, s, -np.inf)
+    with np.errstate(invalid="ignore"):
+        ref_L = np.logaddexp.reduce(s, axis=-1)
+    np.testing.assert_allclose(L[keep], ref_L[keep], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,length,window,use_bm", [(0, 40, 7, False), (1, 33, -1, True),
+                                                         (0, 40, -1, True), (1, 40, 20, True)])
+def test_sampled_entry_points_follow_window_and_block_mask(causal, length, window, use_bm):
+    N, d, bs = 40, 8, 8
+    nb = N // bs
+    bm = (np.random.default_rng(3).random((nb, nb)) < 0.5).astype(np.uint8)
+    np.fill_diagonal(bm, 1)
+    bm_arg = bm if use_bm else None
+    q, k, v, do = (rand(1, 1, N, d) for _ in range(4))
+    kl = np.array([length])
+    kw = dict(window=window, block_mask=bm_arg, block=bs)
+    o, L = oracle.attn_fwd(q, k, v, 0.5, causal, kv_len=kl, **kw)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.5, causal, kv_len=kl, **kw)
+    rows = np.array([0, 1, 17, 39])
+    o_r, L_r = oracle.fwd_rows(q[0, 0], k[0, 0], v[0, 0], 0.5, causal, length, rows, **kw)
+    np.testing.assert_allclose(o_r, o[0, 0, rows], atol=1e-14)
+    np.testing.assert_allclose(L_r, L[0, 0, rows], atol=1e-14)
+    dq_r = oracle.bwd_dq_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], 0.5, causal, length, rows, **kw)
+    np.testing.assert_allclose(dq_r, dq[0, 0, rows], atol=1e-13)
+    cols = np.array([0, 5, 22, 39])
+    dk_c, dv_c = oracle.bwd_dkdv_cols(q[0, 0], k[0, 0], v[0, 0], do[0, 0], 0.5, causal, length,
+                                      cols, **kw)
+    np.testing.assert_allclose(dk_c, dk[0, 0, cols], atol=1e-13)
+    np.testing.assert_allclose(dv_c, dv[0, 0, cols], atol=1e-13)
