@@ -141,12 +141,25 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
-fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, float* L, int B,
-                       int H, int N, int d, float scale, int causal, const int32_t* kv_len,
-                       fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// window < -1 is invalid; the window and block-mask terms run on the d = 64
+// and d = 128 kernels.
+fa_status check_mask(int d, int window, const uint8_t* block_mask) {
+  if (window < -1) return FA_ERR_INVALID_ARG;
+  if ((window >= 0 || block_mask != nullptr) && d == 256) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                   int N, int d, float scale, int causal, const int32_t* kv_len, int window,
+                   const uint8_t* block_mask, fa_stream_t stream) {
   if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
+  if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4) ||
       (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
@@ -172,13 +185,32 @@ fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, flo
   a.n_qtiles = (N + 127) / 128;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.window = window;
+  a.bmask = block_mask;
+  a.nb = (N + 127) / 128;
   if (fa::launch_fwd(d, tq, tk, tv, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                       int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                       fa_stream_t stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, -1, nullptr, stream);
+}
+
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
                  int N, int d, float scale, int causal, fa_stream_t stream) {
-  return fa_fwd_kvlen(Q, K, V, O, L, B, H, N, d, scale, causal, nullptr, stream);
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, nullptr, -1, nullptr, stream);
+}
+
+fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                        int window, const uint8_t* block_mask, fa_stream_t stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, window, block_mask, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -211,11 +243,13 @@ fa_status fa_bwd_prepare(const void* O, const void* dO, int B, int H, int N, int
 // Shared validation and argument block of the two recompute kernels.
 static fa_status bwd_args(const void* Q, const void* K, const void* V, const void* dO,
                           const float* L, int B, int H, int N, int d, float scale, int causal,
-                          const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
+                          const int32_t* kv_len, int window, const uint8_t* block_mask,
+                          const void* workspace, size_t workspace_bytes,
                           fa::BwdArgs* a, EncodeTiledFn* enc) {
   if (!Q || !K || !V || !dO || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
+  if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) ||
       !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
@@ -239,18 +273,22 @@ static fa_status bwd_args(const void* Q, const void* K, const void* V, const voi
   a->scale = scale;
   a->scale_log2 = scale * kLog2e;
   a->causal = causal ? 1 : 0;
+  a->window = window;
+  a->bmask = block_mask;
+  a->nb = (N + 127) / 128;
   return FA_OK;
 }
 
-fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO,
-                      const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
-                      int causal, const int32_t* kv_len, const void* workspace,
-                      size_t workspace_bytes, fa_stream_t stream) {
+static fa_status dkdv_impl(const void* Q, const void* K, const void* V, const void* dO,
+                           const float* L, void* dK, void* dV, int B, int H, int N, int d,
+                           float scale, int causal, const int32_t* kv_len, int window,
+                           const uint8_t* block_mask, const void* workspace,
+                           size_t workspace_bytes, fa_stream_t stream) {
   if (!dK || !dV || !aligned(dK, 16) || !aligned(dV, 16)) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   EncodeTiledFn enc;
-  fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, workspace,
-                          workspace_bytes, &a, &enc);
+  fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, window, block_mask,
+                          workspace, workspace_bytes, &a, &enc);
   if (st != FA_OK) return st;
   a.dK = static_cast<uint16_t*>(dK);
   a.dV = static_cast<uint16_t*>(dV);
@@ -264,15 +302,16 @@ fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* d
   return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, const float* L,
-                    void* dQ, int B, int H, int N, int d, float scale, int causal,
-                    const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
-                    fa_stream_t stream) {
+static fa_status dq_impl(const void* Q, const void* K, const void* V, const void* dO,
+                         const float* L, void* dQ, int B, int H, int N, int d, float scale,
+                         int causal, const int32_t* kv_len, int window,
+                         const uint8_t* block_mask, const void* workspace,
+                         size_t workspace_bytes, fa_stream_t stream) {
   if (!dQ || !aligned(dQ, 16)) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   EncodeTiledFn enc;
-  fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, workspace,
-                          workspace_bytes, &a, &enc);
+  fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, window, block_mask,
+                          workspace, workspace_bytes, &a, &enc);
   if (st != FA_OK) return st;
   a.n_qtiles = (N + 127) / 128;
   CUtensorMap tq, tk, tv, tdo, tdq;
@@ -285,14 +324,16 @@ fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO,
                                                                               : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                 float scale, int causal, const int32_t* kv_len, void* workspace,
-                 size_t workspace_bytes, fa_stream_t stream) {
+static fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
+                          const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                          int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                          int window, const uint8_t* block_mask, void* workspace,
+                          size_t workspace_bytes, fa_stream_t stream) {
   if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV || !workspace)
     return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
+  if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
       !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
       !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
@@ -300,11 +341,44 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
   if ((st = fa_bwd_prepare(O, dO, B, H, N, d, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
-  if ((st = fa_bwd_dkdv(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, workspace,
-                        workspace_bytes, stream)) != FA_OK)
+  if ((st = dkdv_impl(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, window,
+                      block_mask, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
-  return fa_bwd_dq(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, workspace,
-                   workspace_bytes, stream);
+  return dq_impl(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, window, block_mask,
+                 workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO,
+                      const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                      int causal, const int32_t* kv_len, const void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream) {
+  return dkdv_impl(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, -1, nullptr,
+                   workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, const float* L,
+                    void* dQ, int B, int H, int N, int d, float scale, int causal,
+                    const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+  return dq_impl(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, -1, nullptr, workspace,
+                 workspace_bytes, stream);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                 float scale, int causal, const int32_t* kv_len, void* workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, -1, nullptr,
+                  workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                        int window, const uint8_t* block_mask, void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, window,
+                  block_mask, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_check_error(fa_stream_t stream) {

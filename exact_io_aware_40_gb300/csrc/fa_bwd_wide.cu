@@ -28,6 +28,7 @@
 //   Issue order per step: dP_{j+1} (after dP_j is read), dQ_j (after dS_j),
 //   S_{j+2} (into S_j's buffer, after dQ_j has read dS_j).
 #include "kernels.h"
+#include "masks.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -132,8 +133,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const int i_start = a.causal ? kt : 0;
-  const int n_iter = (k0 >= kv_limit) ? 0 : a.n_qtiles - i_start;
+  // Query blocks that see this key block: a range from the masks, thinned by
+  // column kt of the block mask; every role walks it in the same order.
+  int ilo, ihi;
+  query_block_range(kt, a.n_qtiles, kv_limit, a.causal, a.window, &ilo, &ihi);
+  const uint8_t* bmc = a.bmask ? a.bmask + kt : nullptr;  // column kt, stride nb
+  volatile int* n_steps = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+  if (warp == 3) {
+    const int n = count_blocks(bmc, a.nb, ilo, ihi);
+    if (lane == 0) *n_steps = n;
+  }
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
@@ -167,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
+  const int n_iter = *n_steps;
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
@@ -183,9 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int last[W::kSt];
       for (int t = 0; t < W::kSt; ++t) last[t] = -1;
-      for (int it = 0; it < n_iter; ++it) {
+      int qb = next_block(bmc, a.nb, ilo, ihi);
+      for (int it = 0; it < n_iter; ++it, qb = next_block(bmc, a.nb, qb + 1, ihi)) {
         const int st = it % W::kSt;
-        const int q0 = (i_start + it) * kT;
+        const int q0 = qb * kT;
         if (it >= W::kSt &&
             !__all_sync(0xffffffffu, mbar_wait(bar_qdo_empty(st), ((it / W::kSt) & 1) ^ 1, ab)))
           break;
@@ -210,9 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------ row terms L, D
     // Off the Q/dO ring, up to kLdSt steps ahead of the softmax warpgroups.
     const long long rbase = static_cast<long long>(bh) * a.N;
-    for (int it = 0; it < n_iter; ++it) {
+    int qb = next_block(bmc, a.nb, ilo, ihi);
+    for (int it = 0; it < n_iter; ++it, qb = next_block(bmc, a.nb, qb + 1, ihi)) {
       const int st = it % C::kLdSt;
-      const int q0 = (i_start + it) * kT;
+      const int q0 = qb * kT;
       if (it >= C::kLdSt &&
           !__all_sync(0xffffffffu, mbar_wait(bar_ld_empty(st), ((it / C::kLdSt) & 1) ^ 1, ab)))
         break;
@@ -294,9 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t cs = C::kColS + 64u * x, cdp = C::kColdP + 64u * x;
     const bool key_ok = key < kv_limit;
     bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
+    int qb = next_block(bmc, a.nb, ilo, ihi);
+    for (int it = 0; it < n_iter; ++it, qb = next_block(bmc, a.nb, qb + 1, ihi)) {
       const int lst = it % C::kLdSt;
-      const int q0 = (i_start + it) * kT + 64 * x;  // first query column of this half
+      const int q0 = qb * kT + 64 * x;  // first query column of this half
       const float* L2 = sLD + lst * 256 + 64 * x;
       const float* Dv = sLD + lst * 256 + 128 + 64 * x;
       // ---- P^T: on the critical path (S^T -> P^T -> dV -> next S^T)
@@ -306,7 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float p[64];
       if (ok1) {
         tc_fence_after();
-        const bool need_mask = !key_ok || (q0 + 64 > a.N) || (a.causal && q0 < k0 + kT - 1);
+        const bool band = (a.causal != 0) | (a.window >= 0);
+        const bool need_mask = !key_ok || (q0 + 64 > a.N) || (band && q0 < k0 + kT - 1) ||
+                               (a.window >= 0 && k0 < q0 + 63 - a.window);
         uint32_t sr[2][32];
         tmem_ld32(tl + cs, sr[0]);
         tmem_ld32(tl + cs + 32, sr[1]);
@@ -320,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
             const int qg = q0 + e;
-            const bool keep = key_ok & (qg < a.N) & !((a.causal != 0) & (key > qg));
+            const bool keep = (qg < a.N) & visible(qg, key, kv_limit, a.causal, a.window);
             p[e] = keep ? p[e] : 0.f;
           }
         }
@@ -476,8 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  int T = (kv_limit + kT - 1) / kT;
-  if (a.causal) T = min(T, qt + 1);
+  // Key blocks this query block sees: a range from the masks, thinned by row
+  // qt of the block mask; every role walks it in the same order.
+  int jlo, jhi;
+  key_block_range(qt, kv_limit, a.causal, a.window, &jlo, &jhi);
+  const uint8_t* bmr = a.bmask ? a.bmask + static_cast<long long>(qt) * a.nb : nullptr;
+  volatile int* n_steps = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+  if (warp == 3) {
+    const int n = count_blocks(bmr, 1, jlo, jhi);
+    if (lane == 0) *n_steps = n;
+  }
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
@@ -513,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
+  const int T = *n_steps;
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
@@ -527,18 +551,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int lastk[C::kKSt], lastv[C::kVSt];
       for (int s = 0; s < C::kKSt; ++s) lastk[s] = -1;
       for (int s = 0; s < C::kVSt; ++s) lastv[s] = -1;
-      for (int j = 0; j < T; ++j) {
+      int kb = next_block(bmr, 1, jlo, jhi);
+      for (int j = 0; j < T; ++j, kb = next_block(bmr, 1, kb + 1, jhi)) {
         const int sk = j % C::kKSt, sv = j % C::kVSt;
         if (j >= C::kKSt && !mbar_wait(bar_kempty(sk), ((j / C::kKSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_kfull(sk), W::kTile);
         for (int c = 0; c < W::kAtoms; ++c)
-          tma_load_3d(sK + sk * W::kTile + c * 16384, &tmK, c * 64, j * kT, bh, bar_kfull(sk),
+          tma_load_3d(sK + sk * W::kTile + c * 16384, &tmK, c * 64, kb * kT, bh, bar_kfull(sk),
                       pol_kv);
         lastk[sk] = j;
         if (j >= C::kVSt && !mbar_wait(bar_vempty(sv), ((j / C::kVSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_vfull(sv), W::kTile);
         for (int c = 0; c < W::kAtoms; ++c)
-          tma_load_3d(sV + sv * W::kTile + c * 16384, &tmV, c * 64, j * kT, bh, bar_vfull(sv),
+          tma_load_3d(sV + sv * W::kTile + c * 16384, &tmV, c * 64, kb * kT, bh, bar_vfull(sv),
                       pol_kv);
         lastv[sv] = j;
       }
@@ -621,14 +646,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float L2 = grow < a.N ? a.L[ridx] * kLog2e : 0.f;
     const float Dr = grow < a.N ? a.D[ridx] : 0.f;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
+    int kb = next_block(bmr, 1, jlo, jhi);
+    for (int j = 0; j < T; ++j, kb = next_block(bmr, 1, kb + 1, jhi)) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s(j & 1), (j >> 1) & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int key0 = j * kT + 64 * x;  // first key column of this half
-      const bool need_mask = (key0 + 64 > kv_limit) || (a.causal && key0 + 63 > q0);
+      const int key0 = kb * kT + 64 * x;  // first key column of this half
+      const bool band = (a.causal != 0) | (a.window >= 0);
+      const bool need_mask = (key0 + 64 > kv_limit) || (band && key0 + 63 > q0) ||
+                             (a.window >= 0 && key0 < q0 + kT - 1 - a.window);
       uint32_t sr[2][32];
       tmem_ld32(tl + C::kColS + 128u * (j & 1) + 64u * x, sr[0]);
       tmem_ld32(tl + C::kColS + 128u * (j & 1) + 64u * x + 32, sr[1]);
@@ -646,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const int key = key0 + e;
-          const bool keep = (key < kv_limit) & !((a.causal != 0) & (key > grow));
+          const bool keep = visible(grow, key, kv_limit, a.causal, a.window);
           p[e] = keep ? p[e] : 0.f;
         }
       }

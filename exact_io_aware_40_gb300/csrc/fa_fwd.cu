@@ -30,7 +30,10 @@
 // Loop order: query block outer (per CTA), key block inner, so O stays in TMEM
 // for the whole loop; the study notes' K/V-outer order computes the same
 // result (they only differ in which operand is reused on chip).
+#include <type_traits>
+
 #include "kernels.h"
+#include "masks.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -39,8 +42,8 @@ namespace {
 constexpr int kBR = 128;      // query rows per block (MMA M)
 constexpr int kBC = 128;      // keys per block (MMA N of S, K of PV)
 constexpr int kThreads = 384;
-constexpr int kRegsLow = 56;    // warps 0-3 (producer, MMA) after setmaxnreg.dec
-constexpr int kRegsHigh = 224;  // softmax warpgroups after setmaxnreg.inc
+constexpr int kRegsLow = 64;    // warps 0-3 (producer, MMA) after setmaxnreg.dec
+constexpr int kRegsHigh = 216;  // softmax warpgroups after setmaxnreg.inc
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 8
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -58,8 +61,9 @@ struct Cfg {
   // q_full[2], k_full[], k_empty[], v_full[], v_empty[], s_full[2], p_full[2],
   // o_final[2], drain
   static constexpr int kNumBar = 2 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1;
+  // misc: tmem slot, abort flag, then the key-block walk (TA, TB, lo[2], hi[2], ulo, uhi)
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
-  static constexpr int kUsed = kOffMisc + 16;
+  static constexpr int kUsed = kOffMisc + 48;
   static constexpr int kSmemBytes = kUsed + 1024;  // + alignment of the base
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kColO = 256;
@@ -124,12 +128,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const int kv_tiles = (kv_limit + kBC - 1) / kBC;
   const bool hasB = qtA + 1 < a.n_qtiles;
-  // key blocks each query block needs
-  const int TA = a.causal ? min(kv_tiles, qtA + 1) : kv_tiles;
-  const int TB = hasB ? (a.causal ? min(kv_tiles, qtA + 2) : kv_tiles) : 0;
-  const int T = max(TA, TB);
+  // Key blocks each query block can see: a range from the key padding, causal
+  // and window terms, thinned by the block mask.  The CTA walks the union of
+  // both blocks' lists in increasing order (each K_j, V_j is loaded once);
+  // block X processes the first T_X entries of the walk, and an entry inside
+  // that prefix that X does not see is computed fully masked.
+  // The walk (T_A, T_B, lo[2], hi[2], ulo, uhi) is set up once by warp 3.
+  int* walk = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
+  if (warp == 3) {
+    int loA, hiA, loB = 0, hiB = 0;
+    key_block_range(qtA, kv_limit, a.causal, a.window, &loA, &hiA);
+    if (hasB) key_block_range(qtA + 1, kv_limit, a.causal, a.window, &loB, &hiB);
+    const int ulo = loB < hiB ? min(loA, loB) : loA;
+    const int uhi = max(hiA, hiB);
+    const uint8_t* bmA = a.bmask ? a.bmask + static_cast<long long>(qtA) * a.nb : nullptr;
+    const uint8_t* bmB = (a.bmask && hasB) ? a.bmask + static_cast<long long>(qtA + 1) * a.nb : nullptr;
+    // T_A, T_B: entry index (+1) of the last block each query block sees.
+    int n = 0, ta = 0, tb = 0;
+    for (int b0 = ulo; b0 < uhi; b0 += 32) {
+      const int kb = b0 + lane;
+      const bool sa = kb < uhi && kb >= loA && kb < hiA && block_on(bmA, 1, kb);
+      const bool sb2 = kb < uhi && kb >= loB && kb < hiB && block_on(bmB, 1, kb);
+      const uint32_t on = __ballot_sync(0xffffffffu, sa || sb2);
+      const int idx = n + __popc(on & ((1u << lane) - 1u));
+      ta = max(ta, sa ? idx + 1 : 0);
+      tb = max(tb, sb2 ? idx + 1 : 0);
+      n += __popc(on);
+    }
+    ta = __reduce_max_sync(0xffffffffu, ta);
+    tb = __reduce_max_sync(0xffffffffu, tb);
+    if (lane == 0) {
+      walk[0] = ta;
+      walk[1] = tb;
+      walk[2] = loA;
+      walk[3] = loB;
+      walk[4] = hiA;
+      walk[5] = hiB;
+      walk[6] = ulo;
+      walk[7] = uhi;
+    }
+  }
 
   if (tid == 0) {
     mbar_init(bar_qfull(0), 1);
@@ -164,6 +203,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
+  const int TA = walk[0], TB = walk[1];
+  const int T = max(TA, TB);
+  // Bounds re-read from shared memory at each use: kept in registers they
+  // push the producer and softmax warps past their register budgets.
+  volatile int* vw = walk;
+  const int ulo = walk[6];
+  auto sees = [&](int x, int kb) -> bool {  // does query block X see key block kb?
+    const uint8_t* row = a.bmask ? a.bmask + static_cast<long long>(qtA + x) * a.nb : nullptr;
+    return kb >= vw[2 + x] && kb < vw[4 + x] && block_on(row, 1, kb);
+  };
+  auto next_kb = [&](int kb) -> int {  // next entry of the walk at or after kb
+    const int uhi = vw[7];
+    while (kb < uhi && !sees(0, kb) && !sees(1, kb)) ++kb;
+    return kb;
+  };
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
@@ -180,18 +234,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_k[C::kKSt], last_v[C::kVSt];
       for (int s = 0; s < C::kKSt; ++s) last_k[s] = -1;
       for (int s = 0; s < C::kVSt; ++s) last_v[s] = -1;
-      for (int j = 0; j < T; ++j) {
+      int kb = next_kb(ulo);
+      for (int j = 0; j < T; ++j, kb = next_kb(kb + 1)) {
         const int ks = j % C::kKSt, vs = j % C::kVSt;
         if (j >= C::kKSt && !mbar_wait(bar_kempty(ks), ((j / C::kKSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_kfull(ks), C::kTileBytes);
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(sK + ks * C::kTileBytes + c * C::kAtomBytes, &tmK, c * 64, j * kBC, bh,
+          tma_load_3d(sK + ks * C::kTileBytes + c * C::kAtomBytes, &tmK, c * 64, kb * kBC, bh,
                       bar_kfull(ks), pol_kv);
         last_k[ks] = j;
         if (j >= C::kVSt && !mbar_wait(bar_vempty(vs), ((j / C::kVSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_vfull(vs), C::kTileBytes);
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(sV + vs * C::kTileBytes + c * C::kAtomBytes, &tmV, c * 64, j * kBC, bh,
+          tma_load_3d(sV + vs * C::kTileBytes + c * C::kAtomBytes, &tmV, c * 64, kb * kBC, bh,
                       bar_vfull(vs), pol_kv);
         last_v[vs] = j;
       }
@@ -282,8 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t scol = 128u * x;
     const uint32_t ocol = C::kColO + static_cast<uint32_t>(HD) * x;
     float m_run = -INFINITY;                // running max, log2 units (scaled)
-    float l_run = 0.f;
+    float l_run = 0.f;                      // row sum of P
+    float lh_run = 0.f;                     // row sum of P rounded to bf16
     bool ok = true;
+    int kb = next_kb(ulo);
     for (int j = 0; j < Tn; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(x), j & 1, ab))) {
         ok = false;
@@ -294,15 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + 32 * c, sr[c]);
       tmem_wait_ld();
-      const int key0 = j * kBC;
-      const bool need_mask = (key0 + kBC > kv_limit) || (a.causal && key0 + kBC - 1 > q0);
-      if (need_mask) {
+      const int key0 = kb * kBC;
+      const bool tile_on = sees(x, kb);  // false: a block of the walk X does not see
+      const bool crossing = !tile_on || tile_crosses(q0, key0, a.N, kv_limit, a.causal, a.window);
+      if (crossing) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int key = key0 + 32 * c + e;
-            const bool keep = (key < kv_limit) & !((a.causal != 0) & (key > grow));
+            const bool keep = tile_on & visible(grow, key, kv_limit, a.causal, a.window);
             sr[c][e] = keep ? sr[c][e] : __float_as_uint(-INFINITY);  // select, no branch
           }
       }
@@ -321,21 +379,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = grow_max ? m_cand : m_run;
       const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float sp[4] = {0.f, 0.f, 0.f, 0.f};  // partial row sums
+      // P = 2^(s * scale * log2e - m) with packed fp32 pairs (one FMA and one
+      // add per two elements).  The row sum of P gives L.  O is divided by a
+      // second sum, lh: in masked tiles it adds P rounded to bf16 -- the
+      // weights the product actually applies to V -- and elsewhere P itself.
+      // A row with fewer than 128 visible keys has no fully visible tile, so
+      // for it lh is exactly the sum of the weights applied, which keeps its O
+      // accurate; for longer rows the two sums differ by far less than the
+      // bf16 rounding of O.
+      const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      float sum_l, sum_h;
+      auto p_tile = [&](auto rounded_sum) {
+        constexpr bool kRounded = decltype(rounded_sum)::value;
+        uint64_t se[2] = {0ull, 0ull}, sh[2] = {0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), a.scale_log2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), a.scale_log2, -m_use));
-          sp[e & 3] += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
+                             scl2, nm2),
+                      t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
+            pk[e] = pack_bf16(p0, p1);
+            se[e & 1] = f2_add(se[e & 1], f2_pack(p0, p1));
+            if constexpr (kRounded) sh[e & 1] = f2_add(sh[e & 1], bf16x2_to_f2(pk[e]));
+          }
+          // P occupies the first 64 columns of the S buffer (2 bf16 per column).
+          tmem_st16(tl + scol + 16 * c, pk);
         }
-        // P occupies the first 64 columns of the S buffer (2 bf16 per column).
-        tmem_st16(tl + scol + 16 * c, pk);
-      }
-      l_run = l_run * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
+        float u0, u1;
+        f2_unpack(f2_add(se[0], se[1]), u0, u1);
+        sum_l = u0 + u1;
+        sum_h = sum_l;
+        if constexpr (kRounded) {
+          f2_unpack(f2_add(sh[0], sh[1]), u0, u1);
+          sum_h = u0 + u1;
+        }
+      };
+      if (crossing)
+        p_tile(std::true_type{});
+      else
+        p_tile(std::false_type{});
+      l_run = l_run * alpha + sum_l;
+      lh_run = lh_run * alpha + sum_h;
       m_run = m_new;
       if (j > 0 && __any_sync(0xffffffffu, grow_max)) {
         // O_X holds P_X(0..j-1) V; every product writing it has completed (see
@@ -354,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pfull(x));
+      kb = next_kb(kb + 1);
     }
     if (ok && Tn > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_ofinal(x), 0, ab));
@@ -363,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = bar_and(1 + x, 128, ok && *abort_flag == 0);
     if (ok && (x == 0 || hasB)) {
       // ---------------------------------------------------------- epilogue
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv_l = lh_run > 0.f ? 1.f / lh_run : 0.f;
       if (grow < a.N) {
         const float Lv = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         a.L[static_cast<long long>(bh) * a.N + grow] = Lv;

@@ -13,6 +13,8 @@
 //   - warp 0: TMA producer (Q once; K_j, V_j through 2-stage rings);
 //     warp 1: tcgen05 issuer; warps 2-5: softmax (thread = query row = TMEM
 //     lane), conditional O rescale, epilogue (O / l via TMA store, L).
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -233,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grow = q0 + row;              // query index
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float m_run = -INFINITY;                // running max, log2 units (scaled)
-    float l_run = 0.f;
+    float l_run = 0.f;                      // row sum of P
+    float lh_run = 0.f;                     // row sum of P rounded to bf16
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int bb = j & 1;
@@ -273,21 +276,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = grow_max ? m_cand : m_run;
       const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float sp[4] = {0.f, 0.f, 0.f, 0.f};  // partial row sums
+      // P with packed fp32 pairs; the row sum of P gives L, and O is divided by
+      // lh, which adds P rounded to bf16 in masked tiles and P elsewhere (so a
+      // row with fewer visible keys than a tile is normalised by exactly the
+      // weights the product applies; see fa_fwd.cu).
+      const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      float sum_l, sum_h;
+      auto p_tile = [&](auto rounded_sum) {
+        constexpr bool kRounded = decltype(rounded_sum)::value;
+        uint64_t se[2] = {0ull, 0ull}, sh[2] = {0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), a.scale_log2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), a.scale_log2, -m_use));
-          sp[e & 3] += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
+                             scl2, nm2),
+                      t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
+            pk[e] = pack_bf16(p0, p1);
+            se[e & 1] = f2_add(se[e & 1], f2_pack(p0, p1));
+            if constexpr (kRounded) sh[e & 1] = f2_add(sh[e & 1], bf16x2_to_f2(pk[e]));
+          }
+          // P occupies the first 64 columns of the S buffer (2 bf16 per column).
+          tmem_st16(tl + s_col(bb) + 16 * c, pk);
         }
-        // P occupies the first 64 columns of the S buffer (2 bf16 per column).
-        tmem_st16(tl + s_col(bb) + 16 * c, pk);
-      }
-      l_run = l_run * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
+        float u0, u1;
+        f2_unpack(f2_add(se[0], se[1]), u0, u1);
+        sum_l = u0 + u1;
+        sum_h = sum_l;
+        if constexpr (kRounded) {
+          f2_unpack(f2_add(sh[0], sh[1]), u0, u1);
+          sum_h = u0 + u1;
+        }
+      };
+      if (need_mask)
+        p_tile(std::true_type{});
+      else
+        p_tile(std::false_type{});
+      l_run = l_run * alpha + sum_l;
+      lh_run = lh_run * alpha + sum_h;
       m_run = m_new;
       if (j > 0 && __any_sync(0xffffffffu, grow_max)) {
         // O holds P_0..P_{j-1} V; rescale it once PV_{j-1} has landed.  (Only
@@ -324,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = bar_and_128(1, ok && *abort_flag == 0);
     if (ok) {
       // ---------------------------------------------------------- epilogue
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv_l = lh_run > 0.f ? 1.f / lh_run : 0.f;
       if (grow < a.N) {
         const float Lv = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         a.L[static_cast<long long>(bh) * a.N + grow] = Lv;

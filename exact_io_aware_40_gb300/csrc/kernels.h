@@ -15,6 +15,9 @@ struct FwdArgs {
   int n_qtiles;         // ceil(N / 128)
   float scale_log2;     // scale * log2(e)
   int causal;
+  int window;           // < 0: none; w >= 0: keys i - w <= j <= i only
+  const uint8_t* bmask; // block mask [nb, nb] (query block, key block) or nullptr
+  int nb;               // ceil(N / 128)
 };
 
 // Forward: grid = n_qtiles * BH CTAs.
@@ -51,6 +54,9 @@ struct BwdArgs {
   float scale;          // softmax scale
   float scale_log2;     // scale * log2(e)
   int causal;
+  int window;           // < 0: none; w >= 0: keys i - w <= j <= i only
+  const uint8_t* bmask; // block mask [nb, nb] (query block, key block) or nullptr
+  int nb;               // ceil(N / 128)
 };
 
 // Query rows per step of the dK/dV kernel (the box height of its Q and dO

@@ -39,9 +39,12 @@ def load_library():
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_kvlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
+    lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp]
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.fa_bwd_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp,
+                                  vp, sz, vp]
     lib.fa_bwd_prepare.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
     lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
@@ -51,7 +54,8 @@ def load_library():
     lib.fa_check_error.argtypes = [vp]
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
-    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_dkdv",
+    for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_fwd_masked", "fa_bwd", "fa_bwd_masked",
+               "fa_bwd_prepare", "fa_bwd_dkdv",
                "fa_bwd_dq", "fa_check_error", "fa_selftest_stalled_wait"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
@@ -112,6 +116,15 @@ def fa_fwd_kvlen(q, k, v, o, L, scale, causal, kv_len, stream=None):
                                        _stream(stream, q)), "fa_fwd_kvlen")
 
 
+def fa_fwd_masked(q, k, v, o, L, scale, causal, kv_len, window, block_mask, stream=None):
+    """fa_fwd_masked; window is an int (-1: none), block_mask a CUDA uint8
+    [ceil(N/128), ceil(N/128)] tensor or None."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d,
+                                        float(scale), int(bool(causal)), _ptr(kv_len), int(window),
+                                        _ptr(block_mask), _stream(stream, q)), "fa_fwd_masked")
+
+
 def fa_bwd_workspace_bytes(B, H, N, d):
     return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
 
@@ -123,6 +136,17 @@ def fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stre
                                  _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                                  _ptr(kv_len), _ptr(workspace), workspace.numel(),
                                  _stream(stream, q)), "fa_bwd")
+
+
+def fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
+                  workspace, stream=None):
+    """fa_bwd_masked on torch tensors (masks as in fa_fwd_masked)."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                        int(bool(causal)), _ptr(kv_len), int(window),
+                                        _ptr(block_mask), _ptr(workspace), workspace.numel(),
+                                        _stream(stream, q)), "fa_bwd_masked")
 
 
 def fa_bwd_prepare(o, do, workspace, stream=None):
@@ -178,8 +202,22 @@ def fa_check_error(stream=None, device=None):
 
 # ------------------------------------------------------------------ convenience
 
-def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=None, stream=None):
-    """Exact attention forward.  Returns (O bf16 [B,H,N,d], L fp32 [B,H,N])."""
+MASK_BLOCK = 128  # block size of block_mask (FA_MASK_BLOCK)
+
+
+def _expect_mask(block_mask, N):
+    import torch
+    if block_mask is not None:
+        nb = (N + MASK_BLOCK - 1) // MASK_BLOCK
+        _expect(block_mask, "block_mask", torch.uint8, (nb, nb))
+
+
+def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=None, stream=None,
+                  window=-1, block_mask=None):
+    """Exact attention forward.  Returns (O bf16 [B,H,N,d], L fp32 [B,H,N]).
+
+    window (int, -1 = none) and block_mask (CUDA uint8 [ceil(N/128)]^2 or None)
+    select the sliding-window and block-sparse mask terms of fa_fwd_masked."""
     import torch
     B, H, N, d = _shape(q)
     for t, nm in ((q, "q"), (k, "k"), (v, "v")):
@@ -192,12 +230,16 @@ def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if kv_len is not None:
         _expect(kv_len, "kv_len", torch.int32, (B,))
-    fa_fwd_kvlen(q, k, v, out, lse, scale, causal, kv_len, stream)
+    if window >= 0 or block_mask is not None:
+        _expect_mask(block_mask, N)
+        fa_fwd_masked(q, k, v, out, lse, scale, causal, kv_len, window, block_mask, stream)
+    else:
+        fa_fwd_kvlen(q, k, v, out, lse, scale, causal, kv_len, stream)
     return out, lse
 
 
 def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, workspace=None,
-                  stream=None):
+                  stream=None, window=-1, block_mask=None):
     """Exact attention backward.  Returns (dQ, dK, dV), bf16 [B,H,N,d]."""
     import torch
     B, H, N, d = _shape(q)
@@ -212,5 +254,10 @@ def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, work
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream)
+    if window >= 0 or block_mask is not None:
+        _expect_mask(block_mask, N)
+        fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
+                      workspace, stream)
+    else:
+        fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream)
     return dq, dk, dv

@@ -12,7 +12,7 @@ arithmetic and IEEE fp64 are used, so an x86 host and an Arm host draw the
 same bits (up to a last-ulp libm difference in log/cos/sin that the fp32 and
 bf16 roundings almost always absorb).
 
-Streams: tensor ids Q=0, K=1, V=2, dO=3, key-padding lengths=4.  A workload
+Streams: tensor ids Q=0, K=1, V=2, dO=3, key-padding lengths=4, block masks=5.  A workload
 with index ``k`` in the configuration list uses seed ``1000 + k``.
 """
 import numpy as np
@@ -21,7 +21,7 @@ GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-STREAM = {"Q": 0, "K": 1, "V": 2, "dO": 3, "kv_len": 4}
+STREAM = {"Q": 0, "K": 1, "V": 2, "dO": 3, "kv_len": 4, "block_mask": 5}
 SEED_BASE = 1000
 
 
@@ -90,6 +90,17 @@ def kv_lengths(seed, B, lo, hi):
     """Per-sequence key lengths, uniform integers in [lo, hi] (int32 [B])."""
     u = uint64_stream(seed, STREAM["kv_len"], B)
     return (np.uint64(lo) + u % np.uint64(hi - lo + 1)).astype(np.int32)
+
+
+def block_mask(seed, nb, density, diagonal=True):
+    """Random [nb, nb] uint8 block mask: each (query block, key block) pair is
+    kept with probability `density`; `diagonal` keeps every diagonal pair."""
+    u = uint64_stream(seed, STREAM["block_mask"], nb * nb)
+    uni = (u >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    m = (uni < density).astype(np.uint8).reshape(nb, nb)
+    if diagonal:
+        np.fill_diagonal(m, 1)
+    return m
 
 
 def attention_inputs(seed, B, H, N, d, with_dout=True):

@@ -81,6 +81,31 @@ fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, flo
                        fa_stream_t stream);
 
 /*
+ * Forward with two more mask terms, the pages' extensions of the method:
+ *   window      : -1 = none.  w >= 0 keeps key j for query i only when
+ *                 i - w <= j <= i (local causal band; the bxzpzcl.cn article
+ *                 names sliding-window attention among the supported features,
+ *                 section "高级功能配置").
+ *   block_mask  : NULL = none, or a DEVICE uint8 array [nb, nb], nb =
+ *                 ceil(N / FA_MASK_BLOCK), row-major over (query block, key
+ *                 block) pairs of FA_MASK_BLOCK x FA_MASK_BLOCK positions,
+ *                 shared by every batch and head; 0 leaves the pair out
+ *                 (block-sparse attention: the paper's abstract; fmread.com
+ *                 summary, section 六 item 3).  The caller owns it; it is read
+ *                 while the enqueued work runs.
+ * All mask terms intersect (causal, kv_len, window, block mask).  Pairs the
+ * block mask leaves out are never computed: the kernels visit only the
+ * blocks a query block (or key block) keeps.  A query that keeps no key gets
+ * O = 0, L = -inf.
+ * Errors: window < -1 gives FA_ERR_INVALID_ARG; window >= 0 or a block mask
+ * with d = 256 gives FA_ERR_UNSUPPORTED.  Otherwise as fa_fwd_kvlen.
+ */
+#define FA_MASK_BLOCK 128
+fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                        int window, const uint8_t* block_mask, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: the fp32 [B, H, N] row terms
  * D_i = sum_c dO_ic O_ic, rounded up to 256 bytes.  Returns 0 for invalid
  * sizes.
@@ -104,6 +129,17 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
                  float scale, int causal, const int32_t* kv_len, void* workspace,
                  size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_bwd with the window and block-mask terms of fa_fwd_masked (same meaning,
+ * same errors); O and L must come from fa_fwd_masked with the same masks.
+ * Key blocks (and query blocks) the masks leave out are skipped.
+ */
+fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                        int window, const uint8_t* block_mask, void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * The three stages fa_bwd enqueues, for callers that want to schedule or time

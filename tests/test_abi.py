@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_dkdv",
               "fa_bwd_dq", "fa_bwd_workspace_bytes", "fa_check_error", "fa_status_string",
-              "fa_selftest_stalled_wait", "fa_bwd_noalloc"):
+              "fa_selftest_stalled_wait", "fa_bwd_noalloc", "fa_fwd_masked", "fa_bwd_masked"):
         assert n in names
 
 
@@ -102,3 +102,20 @@ def test_backward_stages_reject_invalid_arguments(lib):
     # the no-allocation variant validates sizes before touching its scratch
     assert lib.fa_bwd_noalloc(*([fake] * 9), 1, 1, 128, 96, f(0.1), 0, null, null) == 2
     assert lib.fa_bwd_noalloc(*([fake] * 9), 0, 1, 128, 64, f(0.1), 0, null, null) == 1
+
+
+def test_masked_entry_points_validate_the_mask_terms(lib):
+    fake, null, f = ctypes.c_void_p(0x10000), ctypes.c_void_p(0), ctypes.c_float
+    fwd = lambda d, window, bm: lib.fa_fwd_masked(*([fake] * 5), 1, 1, 256, d, f(0.1), 1, null,
+                                                   window, bm, null)
+    bwd = lambda d, window, bm: lib.fa_bwd_masked(*([fake] * 9), 1, 1, 256, d, f(0.1), 1, null,
+                                                   window, bm, fake, 1 << 20, null)
+    for call in (fwd, bwd):
+        assert call(64, -2, null) == 1          # window below -1
+        assert call(256, 8, null) == 2          # window on the d = 256 kernels
+        assert call(256, -1, fake) == 2         # block mask on the d = 256 kernels
+        assert call(96, 8, null) == 2           # head dim
+    assert lib.fa_fwd_masked(null, *([fake] * 4), 1, 1, 256, 64, f(0.1), 1, null, 4, null,
+                             null) == 1
+    assert lib.fa_bwd_masked(*([fake] * 9), 1, 1, 256, 64, f(0.1), 1, null, 4, null, fake, 16,
+                             null) == 1          # short workspace
