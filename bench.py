@@ -12,6 +12,13 @@ dQ); non-causal P = B*H*N^2, causal P = B*H*N(N+1)/2.  The dQ kernel recomputes
 QK^T and dP a second time; those 4*d*P are not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--mask window:W | --mask blocksparse]
+
+--mask measures the sliding-window or block-sparse variant instead (same
+inputs; one step = fa_fwd_masked + fa_bwd_masked): window:W keeps keys
+i - W .. i of each query; blocksparse keeps, over 128 x 128 blocks, a band of
+three blocks around the diagonal plus the first four key blocks (a
+local + global layout).  FLOPs count only the pairs the mask keeps.
 
 Under torchrun each rank runs the same workload on its own GPU (independent
 replicas, no collective on the data path); rank 0 prints one JSON line.
@@ -194,6 +201,189 @@ def run_reference(args, rank):
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- masked variants
+
+def mask_case(spec, n=None):
+    """(label, causal, window, block mask [nb, nb] uint8 or None, visible pairs
+    per head) of a --mask spec on the first n tokens (default N)."""
+    import numpy as np
+    n = N if n is None else n
+    if spec.startswith("window:"):
+        w = int(spec.split(":", 1)[1])
+        if w < 0:
+            raise ValueError("window must be >= 0")
+        i = np.arange(n, dtype=np.int64)
+        per_head = int(np.minimum(i, w).sum() + n)
+        return "sliding window w=%d (keys i-w..i)" % w, 1, w, None, per_head
+    if spec == "blocksparse":
+        nb = (n + 127) // 128
+        i = np.arange(nb)[:, None]
+        j = np.arange(nb)[None, :]
+        bm = ((np.abs(i - j) <= 1) | (j < 4)).astype(np.uint8)
+        # visible pairs: kept blocks, clipped to n tokens
+        sizes = np.minimum(128, n - 128 * np.arange(nb))
+        per_head = int((bm * sizes[:, None] * sizes[None, :]).sum())
+        return ("block-sparse: 3-block band + 4 global key blocks of 128x128", 0, -1, bm,
+                per_head)
+    raise ValueError("unknown --mask %r (window:W or blocksparse)" % spec)
+
+
+def oracle_sample_masked(spec, n_sample, threads):
+    """The oracle on the first n_sample tokens of each head with the same mask
+    terms, forward + backward.  Returns (seconds, FLOPs, description)."""
+    from exact_io_aware_40_gb300 import inputs
+    from oracle import oracle
+    label, causal, window, bm, per_head = mask_case(spec, n_sample)
+    f64 = {k: inputs.bf16_bits_to_f64(v[:, :, :n_sample]) for k, v in workload_bits().items()}
+    scale = 1.0 / math.sqrt(D)
+    kw = dict(window=window, block_mask=bm, block=128, nthreads=threads)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(f64["Q"], f64["K"], f64["V"], scale, causal, **kw)
+    oracle.attn_bwd(f64["Q"], f64["K"], f64["V"], f64["dO"], scale, causal, **kw)
+    secs = time.perf_counter() - t0
+    desc = "first %d of %d tokens of each of the %d heads, %s, fwd+bwd, fp64" % (
+        n_sample, N, H, label)
+    return secs, 14 * D * B * H * per_head, desc
+
+
+def run_masked(args, rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from exact_io_aware_40_gb300 import build as fab, fa
+
+    fab.build()
+    fa.load_library()
+    label, causal, window, bm, per_head = mask_case(args.mask)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    scale = 1.0 / math.sqrt(D)
+    bits = workload_bits()
+    host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for k, v in bits.items()}
+    q, k, v, do = (host[n].to(dev) for n in ("Q", "K", "V", "dO"))
+    bm_dev = None if bm is None else torch.from_numpy(bm).to(dev)
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    L = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd_masked(q, k, v, o, L, scale, causal, None, window, bm_dev, stream=sp)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, None, window, bm_dev, ws,
+                         stream=sp)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    fa.fa_check_error(sp)
+    torch.cuda.synchronize()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_uuid = dev.index
+    sampler = ClockSampler(gpu_uuid)
+    with sampler:
+        torch.cuda.synchronize()
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s_ in range(args.steps):
+            step(evs[s_])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    fa.fa_check_error(sp)
+    ms_step = t0.elapsed_time(t1) / args.steps
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    P = B * H * per_head
+    flops = 14 * D * P
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for n, t in (("o", o), ("L", L), ("dq", dq), ("dk", dk), ("dv", dv))}
+    dev_out = {"o": o, "L": L, "dq": dq, "dk": dk, "dv": dv}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ("Q", "K", "V", "dO"))
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for dst, nm in ((q, "Q"), (k, "K"), (v, "V"), (do, "dO")):
+            dst.copy_(host[nm], non_blocking=True)
+        step()
+        for n in host_out:
+            host_out[n].copy_(dev_out[n], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    fa.fa_check_error(sp)
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = 4 * D * P / (fwd_ms * 1e-3) / 1e12
+    threads = cpu_threads()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        secs, cflops, desc = oracle_sample_masked(args.mask, 4096, threads)
+        cpu = {"value": cflops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 2)}
+    dense = B * H * N * N
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "long-sequence attention B=%d H=%d N=%d d=%d bf16, fwd+bwd, %s"
+                               % (B, H, N, D, label),
+                   "B": B, "H": H, "N": N, "d": D, "causal": causal, "window": window,
+                   "block_mask": None if bm is None else "%dx%d, %d kept" % (bm.shape + (int(bm.sum()),)),
+                   "visible_pairs": P, "visible_fraction": P / dense, "passes": "fwd+bwd",
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (64 MiB per tensor) -- no flush between steps"},
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd_masked (forward kernel, one launch)",
+                     "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "traffic": None,
+                     "peak_source": "bf16_tflops_sustained of %s peaks" % peak_src,
+                     "frac_of_burst_peak": achieved / burst},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": 4 * args.steps,
+        "clocks": sampler.summary(),
+        "per_pass": {"fwd_ms": fwd_ms, "fwd_tflops": 4 * D * P / (fwd_ms * 1e-3) / 1e12,
+                     "bwd_ms": bwd_ms, "bwd_tflops": 10 * D * P / (bwd_ms * 1e-3) / 1e12},
     }
     print(json.dumps(line), flush=True)
 
@@ -383,6 +573,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host cores")
+    ap.add_argument("--mask", default=None,
+                    help="measure a masked variant: window:W or blocksparse")
     ap.add_argument("--heads", type=int, default=16,
                     help="heads of the workload (default 16); fewer heads give the same "
                          "kernels on a smaller device footprint for profiler captures")
@@ -399,6 +591,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.mask:
+        try:
+            mask_case(args.mask)
+        except ValueError as e:
+            ap.error(str(e))
     if args.impl == "reference":
         # the reference arm is the host-side oracle: rank 0 only, no GPU work
         run_reference(args, rank)
@@ -409,7 +606,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
     try:
-        run_ours(args, rank, world)
+        if args.mask:
+            run_masked(args, rank, world)
+        else:
+            run_ours(args, rank, world)
     finally:
         if world > 1:
             import torch.distributed as dist
