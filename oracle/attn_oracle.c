@@ -48,6 +48,20 @@
  * block) pairs of bs x bs positions: pairs with 0 are left out, every other
  * mask still applies inside the pairs kept.
  *
+ * Dropout on the attention weights (the study notes list dropout among the
+ * steps fused into the kernel -- section "Kernel融合" -- without defining it),
+ * read as the usual inverted dropout on P after the softmax normalisation:
+ *     Pd_ij = P_ij * Z_ij / q,   o_i = sum_j Pd_ij v_j,   L unchanged,
+ * Z_ij in {0, 1} kept with probability q = 1 - p.  Z comes from the
+ * counter-based generator Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11), written below from
+ * its definition: counter (j / 8, i, h, b), key (seed low, seed high word);
+ * the call's 128 bits are eight 16-bit values u, value j % 8 (low half of
+ * word (j % 8) / 2 first) deciding key j; Z_ij = [u >= t] with the integer
+ * threshold t = floor(p * 65536), so q = (65536 - t) / 65536 exactly.
+ * Backward with dropout: dPd = dO V^T, dP = dPd o Z / q, D_i = sum_j P_ij dP_ij,
+ * dS = P o (dP - D), dV = Pd^T dO (dQ, dK as above).
+ *
  * Memory: S and P are materialised for a panel of complete rows (all keys of
  * each row), so every softmax is a plain two-pass safe softmax: no online
  * rescaling appears here.  Tensors are contiguous [B, H, N, d] fp64; L and
@@ -62,6 +76,73 @@
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
 #define ORACLE_ERR_NOMEM 2
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 (SC'11): ten rounds of two 32x32->64 multiplications whose  */
+/* high halves are XORed into the other counter words with the round key;   */
+/* the key is bumped by two Weyl constants after every round.               */
+
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        uint64_t m0 = (uint64_t)0xD2511F53u * x0;
+        uint64_t m1 = (uint64_t)0xCD9E8D57u * x2;
+        uint32_t y0 = (uint32_t)(m1 >> 32) ^ x1 ^ k0;
+        uint32_t y1 = (uint32_t)m1;
+        uint32_t y2 = (uint32_t)(m0 >> 32) ^ x3 ^ k1;
+        uint32_t y3 = (uint32_t)m0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+int oracle_philox4x32_10(const unsigned *ctr, const unsigned *key, unsigned *out)
+{
+    if (!ctr || !key || !out) return 1;
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]}, k[2] = {key[0], key[1]}, o[4];
+    philox4x32_10(c, k, o);
+    for (int t = 0; t < 4; ++t) out[t] = o[t];
+    return 0;
+}
+
+/* Dropout of one (batch, head): thr = 0 means none. */
+typedef struct {
+    uint32_t thr;          /* floor(p * 65536) */
+    uint32_t key[2];       /* seed */
+    uint32_t b, h;
+    double inv_q;          /* 65536 / (65536 - thr) */
+} drop_t;
+
+static drop_t make_drop(double p, unsigned long long seed, int64_t b, int64_t h)
+{
+    drop_t z;
+    double t = floor(p * 65536.0);
+    if (t < 0) t = 0;
+    if (t > 65535) t = 65535;
+    z.thr = (uint32_t)t;
+    z.key[0] = (uint32_t)(seed & 0xffffffffu);
+    z.key[1] = (uint32_t)(seed >> 32);
+    z.b = (uint32_t)b;
+    z.h = (uint32_t)h;
+    z.inv_q = 65536.0 / (65536.0 - (double)z.thr);
+    return z;
+}
+
+/* The dropout multiplier Z_ij / q of element (i, j): 0 or 1/q. */
+static double drop_mult(const drop_t *z, int64_t i, int64_t j)
+{
+    if (z->thr == 0) return 1.0;
+    uint32_t ctr[4] = {(uint32_t)(j / 8), (uint32_t)i, z->h, z->b}, out[4];
+    philox4x32_10(ctr, z->key, out);
+    int t = (int)(j % 8);
+    uint32_t w = out[t / 2];
+    uint32_t u = (t % 2) ? (w >> 16) : (w & 0xffffu);
+    return u >= z->thr ? z->inv_q : 0.0;
+}
 
 /* The mask terms of one (batch, head). */
 typedef struct {
@@ -222,6 +303,8 @@ typedef struct {
     int window;
     const unsigned char *bmask;
     int bs;
+    double drop_p;
+    unsigned long long seed;
     double *o, *L;
     int err;
 } fwd_ctx_t;
@@ -235,6 +318,7 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
     int64_t b = bh / c->H;
     int64_t len = c->kv_len ? c->kv_len[b] : N;
     mask_t msk = make_mask(c->causal, len, c->window, c->bmask, c->bs, N);
+    drop_t z = make_drop(c->drop_p, c->seed, b, bh % c->H);
     const double *q = c->q + bh * N * d, *k = c->k + bh * N * d, *v = c->v + bh * N * d;
     double *o = c->o + bh * N * d, *L = c->L + bh * N;
     int64_t R = panel_rows(N);
@@ -256,6 +340,7 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
             for (int64_t j = 0; j < N; ++j) {
                 double pij = p[r * N + j];
                 if (pij == 0.0) continue;
+                pij *= drop_mult(&z, i, j);
                 const double *vj = v + j * d;
                 for (int c2 = 0; c2 < d; ++c2) oi[c2] += pij * vj[c2];
             }
@@ -267,13 +352,14 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
 
 int oracle_attn_fwd(const double *q, const double *k, const double *v, int B, int H,
                     int N, int d, double scale, int causal, const int *kv_len, int window,
-                    const unsigned char *block_mask, int block, double *o, double *L,
-                    int nthreads)
+                    const unsigned char *block_mask, int block, double drop_p,
+                    unsigned long long seed, double *o, double *L, int nthreads)
 {
     if (!q || !k || !v || !o || !L || B < 0 || H < 0 || N < 0 || d < 1) return ORACLE_ERR_ARG;
     if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     fwd_ctx_t c = {q, k, v, H, N, d, scale, causal, kv_len, window, block_mask, block,
-                   o, L, ORACLE_OK};
+                   drop_p, seed, o, L, ORACLE_OK};
     run_pool(fwd_task, &c, (int64_t)B * H, nthreads);
     return c.err;
 }
@@ -291,6 +377,8 @@ typedef struct {
     int window;
     const unsigned char *bmask;
     int bs;
+    double drop_p;
+    unsigned long long seed;
     double *dq, *dk, *dv;
     int err;
 } bwd_ctx_t;
@@ -304,6 +392,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
     int64_t b = bh / c->H;
     int64_t len = c->kv_len ? c->kv_len[b] : N;
     mask_t msk = make_mask(c->causal, len, c->window, c->bmask, c->bs, N);
+    drop_t z = make_drop(c->drop_p, c->seed, b, bh % c->H);
     int64_t off = bh * N * d;
     const double *q = c->q + off, *k = c->k + off, *v = c->v + off, *dout = c->dout + off;
     double *dq = c->dq + off, *dk = c->dk + off, *dv = c->dv + off;
@@ -326,10 +415,10 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
             int64_t i = r0 + r;
             const double *doi = dout + i * d;
             double *prow = p + r * N, *dprow = dp + r * N;
-            /* dP_ij = dO_i . v_j and D_i = sum_j p_ij dP_ij */
+            /* dP_ij = (dO_i . v_j) Z_ij / q and D_i = sum_j p_ij dP_ij */
             double Di = 0.0;
             for (int64_t j = 0; j < N; ++j) {
-                dprow[j] = visible(i, j, &msk) ? dot(doi, v + j * d, d) : 0.0;
+                dprow[j] = visible(i, j, &msk) ? dot(doi, v + j * d, d) * drop_mult(&z, i, j) : 0.0;
                 Di += prow[j] * dprow[j];
             }
             double *dqi = dq + i * d;
@@ -338,13 +427,14 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
                 double pij = prow[j];
                 if (pij == 0.0) continue;
                 double dsij = pij * (dprow[j] - Di);
+                double pdij = pij * drop_mult(&z, i, j);
                 const double *kj = k + j * d;
                 const double *qi = q + i * d;
                 double *dkj = dk + j * d, *dvj = dv + j * d;
                 for (int c2 = 0; c2 < d; ++c2) {
                     dqi[c2] += c->scale * dsij * kj[c2];
                     dkj[c2] += c->scale * dsij * qi[c2];
-                    dvj[c2] += pij * doi[c2];
+                    dvj[c2] += pdij * doi[c2];
                 }
             }
         }
@@ -354,14 +444,15 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
 
 int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
                     int B, int H, int N, int d, double scale, int causal, const int *kv_len,
-                    int window, const unsigned char *block_mask, int block,
-                    double *dq, double *dk, double *dv, int nthreads)
+                    int window, const unsigned char *block_mask, int block, double drop_p,
+                    unsigned long long seed, double *dq, double *dk, double *dv, int nthreads)
 {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H < 0 || N < 0 || d < 1)
         return ORACLE_ERR_ARG;
     if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     bwd_ctx_t c = {q, k, v, dout, H, N, d, scale, causal, kv_len, window, block_mask, block,
-                   dq, dk, dv, ORACLE_OK};
+                   drop_p, seed, dq, dk, dv, ORACLE_OK};
     run_pool(bwd_task, &c, (int64_t)B * H, nthreads);
     return c.err;
 }
@@ -374,12 +465,15 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
 /* o_out[r*d..], L_out[r] for the listed query rows. */
 int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, int d,
                     double scale, int causal, int len, int window,
-                    const unsigned char *block_mask, int block, int nrows, const int *rows,
+                    const unsigned char *block_mask, int block, double drop_p,
+                    unsigned long long seed, int b, int h, int nrows, const int *rows,
                     double *o_out, double *L_out)
 {
     if (!q || !k || !v || !rows || !o_out || !L_out || N < 1 || d < 1) return ORACLE_ERR_ARG;
     if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     mask_t msk = make_mask(causal, len, window, block_mask, block, N);
+    drop_t z = make_drop(drop_p, seed, b, h);
     double *s = (double *)malloc(sizeof(double) * (size_t)N);
     double *p = (double *)malloc(sizeof(double) * (size_t)N);
     if (!s || !p) { free(s); free(p); return ORACLE_ERR_NOMEM; }
@@ -391,7 +485,8 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, in
         for (int c = 0; c < d; ++c) o_out[(int64_t)r * d + c] = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             if (p[j] == 0.0) continue;
-            for (int c = 0; c < d; ++c) o_out[(int64_t)r * d + c] += p[j] * v[j * d + c];
+            double pd = p[j] * drop_mult(&z, i, j);
+            for (int c = 0; c < d; ++c) o_out[(int64_t)r * d + c] += pd * v[j * d + c];
         }
         L_out[r] = lse;
     }
@@ -403,12 +498,15 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v, int N, in
  * row of P and dP). */
 int oracle_bwd_dq_rows(const double *q, const double *k, const double *v, const double *dout,
                        int N, int d, double scale, int causal, int len, int window,
-                       const unsigned char *block_mask, int block, int nrows,
+                       const unsigned char *block_mask, int block, double drop_p,
+                       unsigned long long seed, int b, int h, int nrows,
                        const int *rows, double *dq_out)
 {
     if (!q || !k || !v || !dout || !rows || !dq_out || N < 1 || d < 1) return ORACLE_ERR_ARG;
     if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     mask_t msk = make_mask(causal, len, window, block_mask, block, N);
+    drop_t z = make_drop(drop_p, seed, b, h);
     double *s = (double *)malloc(sizeof(double) * (size_t)N);
     double *p = (double *)malloc(sizeof(double) * (size_t)N);
     double *dp = (double *)malloc(sizeof(double) * (size_t)N);
@@ -421,7 +519,7 @@ int oracle_bwd_dq_rows(const double *q, const double *k, const double *v, const 
         const double *doi = dout + i * d;
         double Di = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            dp[j] = visible(i, j, &msk) ? dot(doi, v + j * d, d) : 0.0;
+            dp[j] = visible(i, j, &msk) ? dot(doi, v + j * d, d) * drop_mult(&z, i, j) : 0.0;
             Di += p[j] * dp[j];
         }
         double *dqi = dq_out + (int64_t)r * d;
@@ -444,6 +542,7 @@ typedef struct {
     int d;
     double scale;
     const mask_t *msk;
+    const drop_t *drop;
     double *lse, *D;
 } rowstat_ctx_t;
 
@@ -460,7 +559,8 @@ static void rowstat_task(void *vctx, int64_t i, int worker)
     panel_probs(c->q, c->k, N, d, c->scale, c->msk, i, 1, s, p, &lse);
     double Di = 0.0;
     for (int64_t j = 0; j < N; ++j)
-        if (p[j] != 0.0) Di += p[j] * dot(c->dout + i * d, c->v + j * d, d);
+        if (p[j] != 0.0)
+            Di += p[j] * dot(c->dout + i * d, c->v + j * d, d) * drop_mult(c->drop, i, j);
     c->lse[i] = lse;
     c->D[i] = Di;
     free(s); free(p);
@@ -469,17 +569,20 @@ static void rowstat_task(void *vctx, int64_t i, int worker)
 int oracle_bwd_dkdv_cols(const double *q, const double *k, const double *v,
                          const double *dout, int N, int d, double scale, int causal,
                          int len, int window, const unsigned char *block_mask, int block,
+                         double drop_p, unsigned long long seed, int b, int h,
                          int ncols, const int *cols, double *dk_out,
                          double *dv_out, int nthreads)
 {
     if (!q || !k || !v || !dout || !cols || !dk_out || !dv_out || N < 1 || d < 1)
         return ORACLE_ERR_ARG;
     if (block_mask && block < 1) return ORACLE_ERR_ARG;
+    if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     mask_t msk = make_mask(causal, len, window, block_mask, block, N);
+    drop_t z = make_drop(drop_p, seed, b, h);
     double *lse = (double *)malloc(sizeof(double) * (size_t)N);
     double *D = (double *)malloc(sizeof(double) * (size_t)N);
     if (!lse || !D) { free(lse); free(D); return ORACLE_ERR_NOMEM; }
-    rowstat_ctx_t rc = {q, k, v, dout, N, d, scale, &msk, lse, D};
+    rowstat_ctx_t rc = {q, k, v, dout, N, d, scale, &msk, &z, lse, D};
     run_pool(rowstat_task, &rc, N, nthreads);
     for (int64_t i = 0; i < N; ++i)
         if (isnan(lse[i])) { free(lse); free(D); return ORACLE_ERR_NOMEM; }
@@ -491,14 +594,27 @@ int oracle_bwd_dkdv_cols(const double *q, const double *k, const double *v,
         for (int64_t i = 0; i < N; ++i) {
             if (!visible(i, j, &msk)) continue;
             double pij = exp(scale * dot(q + i * d, k + j * d, d) - lse[i]);
-            double dpij = dot(dout + i * d, v + j * d, d);
+            double mij = drop_mult(&z, i, j);
+            double dpij = dot(dout + i * d, v + j * d, d) * mij;
             double ds = pij * (dpij - D[i]);
             for (int c = 0; c < d; ++c) {
                 dkj[c] += scale * ds * q[i * d + c];
-                dvj[c] += pij * dout[i * d + c];
+                dvj[c] += pij * mij * dout[i * d + c];
             }
         }
     }
     free(lse); free(D);
+    return ORACLE_OK;
+}
+
+/* The dropout multipliers Z_ij / q of one (batch, head), [N, N] row-major
+ * (test access to the same definition the computations above use). */
+int oracle_dropout_mult(int b, int h, int N, double drop_p, unsigned long long seed,
+                        double *out)
+{
+    if (!out || N < 0 || !(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
+    drop_t z = make_drop(drop_p, seed, b, h);
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j < N; ++j) out[i * N + j] = drop_mult(&z, i, j);
     return ORACLE_OK;
 }

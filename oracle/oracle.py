@@ -12,6 +12,9 @@ Mask arguments shared by every function: ``causal``; ``kv_len`` (or the
 per-head ``length``); ``window`` (``w >= 0`` keeps only keys ``i - w <= j <=
 i``; ``-1`` for none); ``block_mask`` (uint8 ``[ceil(N/block), ceil(N/block)]``
 over (query block, key block) pairs, 0 = left out; ``None`` for none).
+Dropout: ``dropout_p`` in [0, 1) and a 64-bit ``seed`` (Philox4x32-10 keyed
+decisions, see attn_oracle.c); the per-head entry points also take the head's
+batch and head index ``b``, ``h`` (they are part of the generator's counter).
 """
 import ctypes
 import os
@@ -51,15 +54,23 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int)
         i, d = ctypes.c_int, ctypes.c_double
         bp = ctypes.POINTER(ctypes.c_ubyte)
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, i, i, i, i, d, i, ip, i, bp, i, dp, dp, i]
-        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, d, i, ip, i, bp, i,
+        up = ctypes.POINTER(ctypes.c_uint)
+        u64 = ctypes.c_ulonglong
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, i, i, i, i, d, i, ip, i, bp, i, d, u64,
+                                        dp, dp, i]
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, d, i, ip, i, bp, i, d, u64,
                                         dp, dp, dp, i]
-        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, i, i, d, i, i, i, bp, i, i, ip, dp, dp]
-        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, bp, i, i, ip, dp]
-        lib.oracle_bwd_dkdv_cols.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, bp, i, i, ip,
-                                             dp, dp, i]
+        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, i, i, d, i, i, i, bp, i, d, u64, i, i, i, ip,
+                                        dp, dp]
+        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, bp, i, d, u64, i, i,
+                                           i, ip, dp]
+        lib.oracle_bwd_dkdv_cols.argtypes = [dp, dp, dp, dp, i, i, d, i, i, i, bp, i, d, u64, i,
+                                             i, i, ip, dp, dp, i]
+        lib.oracle_philox4x32_10.argtypes = [up, up, up]
+        lib.oracle_dropout_mult.argtypes = [i, i, i, d, u64, dp]
         for f in ("oracle_attn_fwd", "oracle_attn_bwd", "oracle_fwd_rows",
-                  "oracle_bwd_dq_rows", "oracle_bwd_dkdv_cols"):
+                  "oracle_bwd_dq_rows", "oracle_bwd_dkdv_cols", "oracle_philox4x32_10",
+                  "oracle_dropout_mult"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -91,8 +102,27 @@ def _check(rc, name):
         raise RuntimeError("oracle %s failed with code %d" % (name, rc))
 
 
+def philox4x32_10(ctr, key):
+    """One Philox4x32-10 call: four 32-bit counter words, two key words."""
+    lib = _load()
+    c = (ctypes.c_uint * 4)(*[int(x) & 0xffffffff for x in ctr])
+    k = (ctypes.c_uint * 2)(*[int(x) & 0xffffffff for x in key])
+    o = (ctypes.c_uint * 4)()
+    _check(lib.oracle_philox4x32_10(c, k, o), "philox4x32_10")
+    return [int(x) for x in o]
+
+
+def dropout_mult(b, h, N, dropout_p, seed):
+    """[N, N] dropout multipliers Z_ij / q of head (b, h): 0 or 1/q."""
+    lib = _load()
+    out = np.empty((N, N), np.float64)
+    _check(lib.oracle_dropout_mult(int(b), int(h), int(N), float(dropout_p), int(seed),
+                                   _f64(out)[1]), "dropout_mult")
+    return out
+
+
 def attn_fwd(q, k, v, scale, causal=False, kv_len=None, nthreads=None, window=-1,
-             block_mask=None, block=128):
+             block_mask=None, block=128, dropout_p=0.0, seed=0):
     """Standard attention forward.  Returns (O [B,H,N,d], L [B,H,N]) in fp64."""
     lib = _load()
     B, H, N, d = q.shape
@@ -107,14 +137,14 @@ def attn_fwd(q, k, v, scale, causal=False, kv_len=None, nthreads=None, window=-1
         kv, kvp = None, None
     bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_attn_fwd(qp, kp, vp, B, H, N, d, float(scale), int(bool(causal)), kvp,
-                             int(window), bmp, int(block),
+                             int(window), bmp, int(block), float(dropout_p), int(seed),
                              _f64(o)[1], _f64(L)[1], int(nthreads or default_threads()))
     _check(rc, "attn_fwd")
     return o, L
 
 
 def attn_bwd(q, k, v, dout, scale, causal=False, kv_len=None, nthreads=None, window=-1,
-             block_mask=None, block=128):
+             block_mask=None, block=128, dropout_p=0.0, seed=0):
     """Gradients of standard attention.  Returns (dQ, dK, dV), fp64 [B,H,N,d]."""
     lib = _load()
     B, H, N, d = q.shape
@@ -131,14 +161,15 @@ def attn_bwd(q, k, v, dout, scale, causal=False, kv_len=None, nthreads=None, win
         kv, kvp = None, None
     bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_attn_bwd(qp, kp, vp, dop, B, H, N, d, float(scale), int(bool(causal)), kvp,
-                             int(window), bmp, int(block),
+                             int(window), bmp, int(block), float(dropout_p), int(seed),
                              _f64(dq)[1], _f64(dk)[1], _f64(dv)[1],
                              int(nthreads or default_threads()))
     _check(rc, "attn_bwd")
     return dq, dk, dv
 
 
-def fwd_rows(q, k, v, scale, causal, length, rows, window=-1, block_mask=None, block=128):
+def fwd_rows(q, k, v, scale, causal, length, rows, window=-1, block_mask=None, block=128,
+             dropout_p=0.0, seed=0, b=0, h=0):
     """O and L rows of ONE head (q, k, v are [N, d]) at the listed query rows."""
     lib = _load()
     N, d = q.shape
@@ -150,13 +181,14 @@ def fwd_rows(q, k, v, scale, causal, length, rows, window=-1, block_mask=None, b
     L = np.empty((len(rows),), np.float64)
     bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_fwd_rows(qp, kp, vp, N, d, float(scale), int(bool(causal)), int(length),
-                             int(window), bmp, int(block), len(rows), rp, _f64(o)[1], _f64(L)[1])
+                             int(window), bmp, int(block), float(dropout_p), int(seed), int(b),
+                             int(h), len(rows), rp, _f64(o)[1], _f64(L)[1])
     _check(rc, "fwd_rows")
     return o, L
 
 
 def bwd_dq_rows(q, k, v, dout, scale, causal, length, rows, window=-1, block_mask=None,
-                block=128):
+                block=128, dropout_p=0.0, seed=0, b=0, h=0):
     """dQ rows of ONE head at the listed query rows."""
     lib = _load()
     N, d = q.shape
@@ -168,14 +200,14 @@ def bwd_dq_rows(q, k, v, dout, scale, causal, length, rows, window=-1, block_mas
     dq = np.empty((len(rows), d), np.float64)
     bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_bwd_dq_rows(qp, kp, vp, dop, N, d, float(scale), int(bool(causal)),
-                                int(length), int(window), bmp, int(block), len(rows), rp,
-                                _f64(dq)[1])
+                                int(length), int(window), bmp, int(block), float(dropout_p),
+                                int(seed), int(b), int(h), len(rows), rp, _f64(dq)[1])
     _check(rc, "bwd_dq_rows")
     return dq
 
 
 def bwd_dkdv_cols(q, k, v, dout, scale, causal, length, cols, nthreads=None, window=-1,
-                  block_mask=None, block=128):
+                  block_mask=None, block=128, dropout_p=0.0, seed=0, b=0, h=0):
     """dK and dV rows of ONE head at the listed key indices."""
     lib = _load()
     N, d = q.shape
@@ -188,7 +220,8 @@ def bwd_dkdv_cols(q, k, v, dout, scale, causal, length, cols, nthreads=None, win
     dv = np.empty((len(cols), d), np.float64)
     bm, bmp = _mask(block_mask, N, block)
     rc = lib.oracle_bwd_dkdv_cols(qp, kp, vp, dop, N, d, float(scale), int(bool(causal)),
-                                  int(length), int(window), bmp, int(block), len(cols), cp,
+                                  int(length), int(window), bmp, int(block), float(dropout_p),
+                                  int(seed), int(b), int(h), len(cols), cp,
                                   _f64(dk)[1], _f64(dv)[1],
                                   int(nthreads or default_threads()))
     _check(rc, "bwd_dkdv_cols")

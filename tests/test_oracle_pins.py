@@ -463,3 +463,136 @@ def test_sampled_entry_points_follow_window_and_block_mask(causal, length, windo
                                       cols, **kw)
     np.testing.assert_allclose(dk_c, dk[0, 0, cols], atol=1e-13)
     np.testing.assert_allclose(dv_c, dv[0, 0, cols], atol=1e-13)
+
+
+# --- dropout ------------------------------------------------------------------
+
+def test_philox4x32_10_known_answers():
+    # Known-answer vectors published with the generator's reference
+    # implementation (Random123): zero counter and key, all-ones counter and
+    # key, and counter/key taken from the hexadecimal digits of pi.
+    assert oracle.philox4x32_10([0, 0, 0, 0], [0, 0]) == [
+        0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+    ones = 0xFFFFFFFF
+    assert oracle.philox4x32_10([ones] * 4, [ones] * 2) == [
+        0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]
+    assert oracle.philox4x32_10([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344],
+                                [0xA4093822, 0x299F31D0]) == [
+        0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]
+
+
+def test_dropout_decisions_follow_the_counter_layout():
+    # Z_ij comes from Philox at counter (j // 8, i, h, b), key (seed low, high),
+    # 16-bit value j % 8 (low half of word (j % 8) // 2 first), kept iff
+    # u >= floor(p * 65536).  Spot-check against direct generator calls.
+    p, seed, b, h, N = 0.3, 0x0123456789ABCDEF, 1, 2, 40
+    m = oracle.dropout_mult(b, h, N, p, seed)
+    thr = int(math.floor(p * 65536))
+    inv_q = 65536.0 / (65536 - thr)
+    for (i, j) in [(0, 0), (0, 7), (3, 8), (17, 33), (39, 39), (5, 22)]:
+        w = oracle.philox4x32_10([j // 8, i, h, b], [seed & 0xFFFFFFFF, seed >> 32])[(j % 8) // 2]
+        u = (w >> 16) if (j % 8) % 2 else (w & 0xFFFF)
+        assert m[i, j] == (inv_q if u >= thr else 0.0)
+
+
+def test_dropout_keep_rate_and_unbiased_scale():
+    p, N = 0.25, 1024
+    ms = [oracle.dropout_mult(b, h, N, p, 777) for b in (0, 1) for h in (0, 3)]
+    keep = np.mean([(m > 0).mean() for m in ms])
+    q = (65536 - math.floor(p * 65536)) / 65536
+    sigma = math.sqrt(q * (1 - q) / (4 * N * N))
+    assert abs(keep - q) < 5 * sigma
+    assert abs(np.mean([m.mean() for m in ms]) - 1.0) < 5 * sigma / q
+    # different heads, batches and rows draw different decisions
+    assert not np.array_equal(ms[0], ms[1]) and not np.array_equal(ms[0], ms[2])
+    assert not np.array_equal(ms[0][0], ms[0][1])
+
+
+def test_dropout_zero_is_no_dropout_and_single_key_closed_form():
+    q, k, v, do = (rand(2, 2, 33, 8) for _ in range(4))
+    o0, L0 = oracle.attn_fwd(q, k, v, 0.5, True)
+    o1, L1 = oracle.attn_fwd(q, k, v, 0.5, True, dropout_p=0.0, seed=99)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(L0, L1)
+    g0 = oracle.attn_bwd(q, k, v, do, 0.5, True)
+    g1 = oracle.attn_bwd(q, k, v, do, 0.5, True, dropout_p=0.0, seed=99)
+    for a, b in zip(g0, g1):
+        np.testing.assert_array_equal(a, b)
+    # one key: P = 1, so O = v * Z/q and L = scale q.k whatever the drop
+    q1, k1, v1 = (rand(1, 3, 1, 6) for _ in range(3))
+    o, L = oracle.attn_fwd(q1, k1, v1, 0.7, False, dropout_p=0.4, seed=5)
+    for h in range(3):
+        mult = oracle.dropout_mult(0, h, 1, 0.4, 5)[0, 0]
+        np.testing.assert_allclose(o[0, h, 0], v1[0, h, 0] * mult, atol=1e-15)
+    np.testing.assert_allclose(L, 0.7 * np.einsum("bhic,bhic->bhi", q1, k1), atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_matches_torch_fp64_autograd_with_the_same_multipliers(causal):
+    # The attention arithmetic with dropout, restated with library operations
+    # (softmax, matmul, autograd) around the oracle's own multiplier matrix.
+    torch = pytest.importorskip("torch")
+    B, H, N, d, p, seed = 2, 2, 21, 8, 0.35, 2024
+    lens = np.array([21, 14])
+    q, k, v, do = (rand(B, H, N, d) for _ in range(4))
+    o, L = oracle.attn_fwd(q, k, v, 0.4, causal, kv_len=lens, dropout_p=p, seed=seed)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.4, causal, kv_len=lens, dropout_p=p, seed=seed)
+    mult = np.stack([np.stack([oracle.dropout_mult(b, h, N, p, seed) for h in range(H)])
+                     for b in range(B)])
+    mask = np.zeros((B, 1, N, N), bool)
+    for b in range(B):
+        mask[b, 0] = visible_mask(N, causal, lens[b])
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    s = 0.4 * tq @ tk.transpose(-1, -2)
+    s = s.masked_fill(~torch.tensor(mask), float("-inf"))
+    P = torch.softmax(s, dim=-1)
+    to = (P * torch.tensor(mult)) @ tv
+    to.backward(torch.tensor(do))
+    np.testing.assert_allclose(o, to.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(L, torch.logsumexp(s, dim=-1).detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
+def test_dropout_backward_matches_central_differences():
+    # With the seed fixed the dropout decisions are fixed, so <dO, O> is a
+    # smooth function of Q, K, V and its gradient is the backward pass.
+    N, d, p, seed = 9, 4, 0.3, 31
+    q, k, v, do = (rand(1, 1, N, d) for _ in range(4))
+    f = lambda q_, k_, v_: float((oracle.attn_fwd(q_, k_, v_, 0.6, True, dropout_p=p,
+                                                  seed=seed)[0] * do).sum())
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.6, True, dropout_p=p, seed=seed)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [xp if n == name else a for n, a in (("q", q), ("k", k), ("v", v))]
+            args_m = [xm if n == name else a for n, a in (("q", q), ("k", k), ("v", v))]
+            num[idx] = (f(*args_p) - f(*args_m)) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_dropout_sampled_entry_points_match_whole_tensor_results():
+    N, d, p, seed = 40, 8, 0.2, 77
+    q, k, v, do = (rand(2, 3, N, d) for _ in range(4))
+    kl = np.array([40, 29])
+    kw = dict(window=11, dropout_p=p, seed=seed)
+    o, L = oracle.attn_fwd(q, k, v, 0.5, True, kv_len=kl, **kw)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.5, True, kv_len=kl, **kw)
+    rows = np.array([0, 1, 17, 39])
+    cols = np.array([0, 5, 22, 39])
+    for b, h in ((0, 0), (1, 2)):
+        qh, kh, vh, doh = q[b, h], k[b, h], v[b, h], do[b, h]
+        ln = int(kl[b])
+        o_r, L_r = oracle.fwd_rows(qh, kh, vh, 0.5, True, ln, rows, b=b, h=h, **kw)
+        np.testing.assert_allclose(o_r, o[b, h, rows], atol=1e-14)
+        np.testing.assert_allclose(L_r, L[b, h, rows], atol=1e-14)
+        dq_r = oracle.bwd_dq_rows(qh, kh, vh, doh, 0.5, True, ln, rows, b=b, h=h, **kw)
+        np.testing.assert_allclose(dq_r, dq[b, h, rows], atol=1e-13)
+        dk_c, dv_c = oracle.bwd_dkdv_cols(qh, kh, vh, doh, 0.5, True, ln, cols, b=b, h=h, **kw)
+        np.testing.assert_allclose(dk_c, dk[b, h, cols], atol=1e-13)
+        np.testing.assert_allclose(dv_c, dv[b, h, cols], atol=1e-13)
