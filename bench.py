@@ -12,13 +12,14 @@ dQ); non-causal P = B*H*N^2, causal P = B*H*N(N+1)/2.  The dQ kernel recomputes
 QK^T and dP a second time; those 4*d*P are not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--mask window:W | --mask blocksparse]
+                    [--mask dense|causal|window:W|blocksparse] [--dropout P]
 
---mask measures the sliding-window or block-sparse variant instead (same
-inputs; one step = fa_fwd_masked + fa_bwd_masked): window:W keeps keys
+--mask measures one variant instead (same inputs; one step = fa_fwd_dropout +
+fa_bwd_dropout with that mask): dense or causal attention; window:W keeps keys
 i - W .. i of each query; blocksparse keeps, over 128 x 128 blocks, a band of
 three blocks around the diagonal plus the first four key blocks (a
-local + global layout).  FLOPs count only the pairs the mask keeps.
+local + global layout).  --dropout P adds dropout with probability P (seed
+fixed).  FLOPs count only the pairs the mask keeps.
 
 Under torchrun each rank runs the same workload on its own GPU (independent
 replicas, no collective on the data path); rank 0 prints one JSON line.
@@ -212,6 +213,9 @@ def mask_case(spec, n=None):
     per head) of a --mask spec on the first n tokens (default N)."""
     import numpy as np
     n = N if n is None else n
+    if spec in ("dense", "causal"):
+        c = int(spec == "causal")
+        return "%s attention" % spec, c, -1, None, (n * (n + 1) // 2 if c else n * n)
     if spec.startswith("window:"):
         w = int(spec.split(":", 1)[1])
         if w < 0:
@@ -229,7 +233,7 @@ def mask_case(spec, n=None):
         per_head = int((bm * sizes[:, None] * sizes[None, :]).sum())
         return ("block-sparse: 3-block band + 4 global key blocks of 128x128", 0, -1, bm,
                 per_head)
-    raise ValueError("unknown --mask %r (window:W or blocksparse)" % spec)
+    raise ValueError("unknown --mask %r (dense, causal, window:W or blocksparse)" % spec)
 
 
 def oracle_sample_masked(spec, n_sample, threads):
@@ -240,7 +244,10 @@ def oracle_sample_masked(spec, n_sample, threads):
     label, causal, window, bm, per_head = mask_case(spec, n_sample)
     f64 = {k: inputs.bf16_bits_to_f64(v[:, :, :n_sample]) for k, v in workload_bits().items()}
     scale = 1.0 / math.sqrt(D)
-    kw = dict(window=window, block_mask=bm, block=128, nthreads=threads)
+    kw = dict(window=window, block_mask=bm, block=128, nthreads=threads,
+              dropout_p=float(_np32(DROPOUT)), seed=DROPOUT_SEED)
+    if DROPOUT > 0:
+        label += ", dropout p=%g" % DROPOUT
     t0 = time.perf_counter()
     oracle.attn_fwd(f64["Q"], f64["K"], f64["V"], scale, causal, **kw)
     oracle.attn_bwd(f64["Q"], f64["K"], f64["V"], f64["dO"], scale, causal, **kw)
@@ -248,6 +255,15 @@ def oracle_sample_masked(spec, n_sample, threads):
     desc = "first %d of %d tokens of each of the %d heads, %s, fwd+bwd, fp64" % (
         n_sample, N, H, label)
     return secs, 14 * D * B * H * per_head, desc
+
+
+DROPOUT = 0.0            # --dropout
+DROPOUT_SEED = 0x0DD5EED
+
+
+def _np32(x):
+    import numpy as np
+    return np.float32(x)
 
 
 def run_masked(args, rank, world):
@@ -259,6 +275,8 @@ def run_masked(args, rank, world):
     fab.build()
     fa.load_library()
     label, causal, window, bm, per_head = mask_case(args.mask)
+    if DROPOUT > 0:
+        label += ", dropout p=%g" % DROPOUT
     dev = torch.device("cuda", torch.cuda.current_device())
     scale = 1.0 / math.sqrt(D)
     bits = workload_bits()
@@ -275,11 +293,12 @@ def run_masked(args, rank, world):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        fa.fa_fwd_masked(q, k, v, o, L, scale, causal, None, window, bm_dev, stream=sp)
+        fa.fa_fwd_dropout(q, k, v, o, L, scale, causal, None, window, bm_dev, DROPOUT,
+                          DROPOUT_SEED, stream=sp)
         if ev is not None:
             ev[1].record(stream)
-        fa.fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, None, window, bm_dev, ws,
-                         stream=sp)
+        fa.fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, None, window, bm_dev,
+                          DROPOUT, DROPOUT_SEED, ws, stream=sp)
         if ev is not None:
             ev[2].record(stream)
 
@@ -368,11 +387,12 @@ def run_masked(args, rank, world):
         "config": {"workload": "long-sequence attention B=%d H=%d N=%d d=%d bf16, fwd+bwd, %s"
                                % (B, H, N, D, label),
                    "B": B, "H": H, "N": N, "d": D, "causal": causal, "window": window,
+                   "dropout_p": DROPOUT,
                    "block_mask": None if bm is None else "%dx%d, %d kept" % (bm.shape + (int(bm.sum()),)),
                    "visible_pairs": P, "visible_fraction": P / dense, "passes": "fwd+bwd",
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (64 MiB per tensor) -- no flush between steps"},
-        "roofline": {"bound": "tensor", "kernel": "fa_fwd_masked (forward kernel, one launch)",
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd_dropout (forward kernel, one launch)",
                      "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                      "traffic": None,
                      "peak_source": "bf16_tflops_sustained of %s peaks" % peak_src,
@@ -574,7 +594,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host cores")
     ap.add_argument("--mask", default=None,
-                    help="measure a masked variant: window:W or blocksparse")
+                    help="measure one variant: dense, causal, window:W or blocksparse")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout probability of the --mask variant (default 0)")
     ap.add_argument("--heads", type=int, default=16,
                     help="heads of the workload (default 16); fewer heads give the same "
                          "kernels on a smaller device footprint for profiler captures")
@@ -591,6 +613,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    global DROPOUT
+    if args.dropout and not args.mask:
+        ap.error("--dropout needs --mask (dense, causal, window:W or blocksparse)")
+    if not 0.0 <= args.dropout < 1.0:
+        ap.error("--dropout must be in [0, 1)")
+    DROPOUT = args.dropout
     if args.mask:
         try:
             mask_case(args.mask)

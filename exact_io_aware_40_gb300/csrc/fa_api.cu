@@ -153,13 +153,35 @@ fa_status check_mask(int d, int window, const uint8_t* block_mask) {
   return FA_OK;
 }
 
+// Dropout parameters of the kernels: the integer keep threshold
+// floor(p * 65536) (0: no dropout) and the unbiased scale 65536 / (65536 - thr).
+struct Drop {
+  uint32_t thr = 0, seed_lo = 0, seed_hi = 0;
+  float scale = 1.f;
+};
+fa_status make_drop(int d, float p, uint64_t seed, Drop* out) {
+  if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;
+  Drop z;
+  const double t = std::floor(static_cast<double>(p) * 65536.0);
+  z.thr = static_cast<uint32_t>(t > 65535.0 ? 65535.0 : t);
+  z.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
+  z.seed_hi = static_cast<uint32_t>(seed >> 32);
+  z.scale = static_cast<float>(65536.0 / (65536.0 - static_cast<double>(z.thr)));
+  if (z.thr != 0 && d == 256) return FA_ERR_UNSUPPORTED;
+  *out = z;
+  return FA_OK;
+}
+
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
                    int N, int d, float scale, int causal, const int32_t* kv_len, int window,
-                   const uint8_t* block_mask, fa_stream_t stream) {
+                   const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                   fa_stream_t stream) {
   if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
+  Drop drop;
+  if ((st = make_drop(d, dropout_p, seed, &drop)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4) ||
       (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
@@ -188,6 +210,10 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.window = window;
   a.bmask = block_mask;
   a.nb = (N + 127) / 128;
+  a.drop_thr = drop.thr;
+  a.seed_lo = drop.seed_lo;
+  a.seed_hi = drop.seed_hi;
+  a.drop_scale = drop.scale;
   if (fa::launch_fwd(d, tq, tk, tv, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -199,18 +225,28 @@ extern "C" {
 fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, float* L, int B,
                        int H, int N, int d, float scale, int causal, const int32_t* kv_len,
                        fa_stream_t stream) {
-  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, -1, nullptr, stream);
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, -1, nullptr, 0.f, 0, stream);
 }
 
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
                  int N, int d, float scale, int causal, fa_stream_t stream) {
-  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, nullptr, -1, nullptr, stream);
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, nullptr, -1, nullptr, 0.f, 0,
+                  stream);
 }
 
 fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B,
                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
                         int window, const uint8_t* block_mask, fa_stream_t stream) {
-  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, window, block_mask, stream);
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, window, block_mask, 0.f, 0,
+                  stream);
+}
+
+fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                         int window, const uint8_t* block_mask, float dropout_p,
+                         uint64_t dropout_seed, fa_stream_t stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, window, block_mask, dropout_p,
+                  dropout_seed, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -244,12 +280,14 @@ fa_status fa_bwd_prepare(const void* O, const void* dO, int B, int H, int N, int
 static fa_status bwd_args(const void* Q, const void* K, const void* V, const void* dO,
                           const float* L, int B, int H, int N, int d, float scale, int causal,
                           const int32_t* kv_len, int window, const uint8_t* block_mask,
-                          const void* workspace, size_t workspace_bytes,
-                          fa::BwdArgs* a, EncodeTiledFn* enc) {
+                          float dropout_p, uint64_t seed, const void* workspace,
+                          size_t workspace_bytes, fa::BwdArgs* a, EncodeTiledFn* enc) {
   if (!Q || !K || !V || !dO || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
+  Drop drop;
+  if ((st = make_drop(d, dropout_p, seed, &drop)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) ||
       !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
@@ -276,19 +314,23 @@ static fa_status bwd_args(const void* Q, const void* K, const void* V, const voi
   a->window = window;
   a->bmask = block_mask;
   a->nb = (N + 127) / 128;
+  a->drop_thr = drop.thr;
+  a->seed_lo = drop.seed_lo;
+  a->seed_hi = drop.seed_hi;
+  a->drop_scale = drop.scale;
   return FA_OK;
 }
 
 static fa_status dkdv_impl(const void* Q, const void* K, const void* V, const void* dO,
                            const float* L, void* dK, void* dV, int B, int H, int N, int d,
                            float scale, int causal, const int32_t* kv_len, int window,
-                           const uint8_t* block_mask, const void* workspace,
-                           size_t workspace_bytes, fa_stream_t stream) {
+                           const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                           const void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   if (!dK || !dV || !aligned(dK, 16) || !aligned(dV, 16)) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   EncodeTiledFn enc;
   fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, window, block_mask,
-                          workspace, workspace_bytes, &a, &enc);
+                          dropout_p, seed, workspace, workspace_bytes, &a, &enc);
   if (st != FA_OK) return st;
   a.dK = static_cast<uint16_t*>(dK);
   a.dV = static_cast<uint16_t*>(dV);
@@ -305,13 +347,13 @@ static fa_status dkdv_impl(const void* Q, const void* K, const void* V, const vo
 static fa_status dq_impl(const void* Q, const void* K, const void* V, const void* dO,
                          const float* L, void* dQ, int B, int H, int N, int d, float scale,
                          int causal, const int32_t* kv_len, int window,
-                         const uint8_t* block_mask, const void* workspace,
-                         size_t workspace_bytes, fa_stream_t stream) {
+                         const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                         const void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   if (!dQ || !aligned(dQ, 16)) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   EncodeTiledFn enc;
   fa_status st = bwd_args(Q, K, V, dO, L, B, H, N, d, scale, causal, kv_len, window, block_mask,
-                          workspace, workspace_bytes, &a, &enc);
+                          dropout_p, seed, workspace, workspace_bytes, &a, &enc);
   if (st != FA_OK) return st;
   a.n_qtiles = (N + 127) / 128;
   CUtensorMap tq, tk, tv, tdo, tdq;
@@ -327,13 +369,15 @@ static fa_status dq_impl(const void* Q, const void* K, const void* V, const void
 static fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
                           const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
                           int H, int N, int d, float scale, int causal, const int32_t* kv_len,
-                          int window, const uint8_t* block_mask, void* workspace,
-                          size_t workspace_bytes, fa_stream_t stream) {
+                          int window, const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                          void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV || !workspace)
     return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
+  Drop drop;
+  if ((st = make_drop(d, dropout_p, seed, &drop)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
       !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
       !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
@@ -342,17 +386,17 @@ static fa_status bwd_impl(const void* Q, const void* K, const void* V, const voi
   if ((st = fa_bwd_prepare(O, dO, B, H, N, d, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
   if ((st = dkdv_impl(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, window,
-                      block_mask, workspace, workspace_bytes, stream)) != FA_OK)
+                      block_mask, dropout_p, seed, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
   return dq_impl(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, window, block_mask,
-                 workspace, workspace_bytes, stream);
+                 dropout_p, seed, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO,
                       const float* L, void* dK, void* dV, int B, int H, int N, int d, float scale,
                       int causal, const int32_t* kv_len, const void* workspace,
                       size_t workspace_bytes, fa_stream_t stream) {
-  return dkdv_impl(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, -1, nullptr,
+  return dkdv_impl(Q, K, V, dO, L, dK, dV, B, H, N, d, scale, causal, kv_len, -1, nullptr, 0.f, 0,
                    workspace, workspace_bytes, stream);
 }
 
@@ -360,8 +404,8 @@ fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO,
                     void* dQ, int B, int H, int N, int d, float scale, int causal,
                     const int32_t* kv_len, const void* workspace, size_t workspace_bytes,
                     fa_stream_t stream) {
-  return dq_impl(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, -1, nullptr, workspace,
-                 workspace_bytes, stream);
+  return dq_impl(Q, K, V, dO, L, dQ, B, H, N, d, scale, causal, kv_len, -1, nullptr, 0.f, 0,
+                 workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
@@ -369,7 +413,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  float scale, int causal, const int32_t* kv_len, void* workspace,
                  size_t workspace_bytes, fa_stream_t stream) {
   return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, -1, nullptr,
-                  workspace, workspace_bytes, stream);
+                  0.f, 0, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
@@ -378,7 +422,17 @@ fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void*
                         int window, const uint8_t* block_mask, void* workspace,
                         size_t workspace_bytes, fa_stream_t stream) {
   return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, window,
-                  block_mask, workspace, workspace_bytes, stream);
+                  block_mask, 0.f, 0, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                         int window, const uint8_t* block_mask, float dropout_p,
+                         uint64_t dropout_seed, void* workspace, size_t workspace_bytes,
+                         fa_stream_t stream) {
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, window,
+                  block_mask, dropout_p, dropout_seed, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_check_error(fa_stream_t stream) {

@@ -28,7 +28,10 @@
 //   Issue order per step: dP_{j+1} (after dP_j is read), dQ_j (after dS_j),
 //   S_{j+2} (into S_j's buffer, after dQ_j has read dS_j).
 #include "kernels.h"
+#include <type_traits>
+
 #include "masks.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -97,7 +100,8 @@ struct KvW {
   static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + HD;
 };
 
-template <int HD>
+// DROP: dropout on P (a separate instantiation, as in the forward).
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
@@ -312,6 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = qb * kT + 64 * x;  // first query column of this half
       const float* L2 = sLD + lst * 256 + 64 * x;
       const float* Dv = sLD + lst * 256 + 128 + 64 * x;
+      // Dropout keep bits of this thread's key for the step's 64 queries of
+      // this half (the warp draws them together), before S^T arrives.
+      uint64_t km = 0;
+      if constexpr (DROP)
+        if (ok)
+          km = keep64_transposed(static_cast<uint32_t>(k0 + quarter * 32), static_cast<uint32_t>(q0),
+                               static_cast<uint32_t>(bh % a.H), static_cast<uint32_t>(b),
+                               a.seed_lo, a.seed_hi, a.drop_thr);
       // ---- P^T: on the critical path (S^T -> P^T -> dV -> next S^T)
       const bool ok1 = ok && __all_sync(0xffffffffu,
                                         mbar_wait(bar_ld_full(lst), (it / C::kLdSt) & 1, ab) &&
@@ -340,8 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         uint32_t w[32];
+        if constexpr (DROP) {
+          // dV takes the dropped weights P Z / q; p itself stays for dS^T.
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+          for (int e = 0; e < 32; ++e)
+            w[e] = pack_bf16((km >> (2 * e)) & 1u ? p[2 * e] * a.drop_scale : 0.f,
+                             (km >> (2 * e + 1)) & 1u ? p[2 * e + 1] * a.drop_scale : 0.f);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+        }
         // P^T over the first half of this warpgroup's S^T columns (read above)
         tmem_st32(tl + cs, w);
         tmem_wait_st();
@@ -366,13 +386,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tl + cdp + 32 * c, dr);
           tmem_wait_ld();
           uint32_t w[16];
+          // dS^T = P^T o (dP^T - D); with dropout dP^T = (V dO^T) Z / q.
+          auto ds_chunk = [&](auto drop) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int qa = 32 * c + 2 * e;
-            const float d0 = p[qa] * (__uint_as_float(dr[2 * e]) - Dv[qa]);
-            const float d1 = p[qa + 1] * (__uint_as_float(dr[2 * e + 1]) - Dv[qa + 1]);
-            w[e] = pack_bf16(d0, d1);
-          }
+            for (int e = 0; e < 16; ++e) {
+              const int qa = 32 * c + 2 * e;
+              float g0 = __uint_as_float(dr[2 * e]), g1 = __uint_as_float(dr[2 * e + 1]);
+              if constexpr (decltype(drop)::value) {
+                g0 = (km >> qa) & 1u ? g0 * a.drop_scale : 0.f;
+                g1 = (km >> (qa + 1)) & 1u ? g1 * a.drop_scale : 0.f;
+              }
+              w[e] = pack_bf16(p[qa] * (g0 - Dv[qa]), p[qa + 1] * (g1 - Dv[qa + 1]));
+            }
+          };
+          if constexpr (DROP)
+            ds_chunk(std::true_type{});
+          else
+            ds_chunk(std::false_type{});
           tmem_st16(tl + cdp + 16 * c, w);  // dS^T over columns this thread has read
         }
         tmem_wait_st();
@@ -454,7 +484,7 @@ struct QW {
   static constexpr uint32_t kColS = 0, kColdP = 256, kColdQ = 384;
 };
 
-template <int HD>
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
@@ -646,14 +676,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float L2 = grow < a.N ? a.L[ridx] * kLog2e : 0.f;
     const float Dr = grow < a.N ? a.D[ridx] : 0.f;
     bool ok = true;
+    const uint32_t hh = static_cast<uint32_t>(bh % a.H), bb = static_cast<uint32_t>(b);
     int kb = next_block(bmr, 1, jlo, jhi);
     for (int j = 0; j < T; ++j, kb = next_block(bmr, 1, kb + 1, jhi)) {
+      const int key0 = kb * kT + 64 * x;  // first key column of this half
+      // Dropout keep bits of this row's 64 keys, drawn before S arrives.
+      uint64_t km = 0;
+      if constexpr (DROP)
+        km = keep32(static_cast<uint32_t>(key0), static_cast<uint32_t>(grow), hh, bb, a.seed_lo,
+                    a.seed_hi, a.drop_thr) |
+             static_cast<uint64_t>(keep32(static_cast<uint32_t>(key0 + 32),
+                                          static_cast<uint32_t>(grow), hh, bb, a.seed_lo,
+                                          a.seed_hi, a.drop_thr))
+                 << 32;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s(j & 1), (j >> 1) & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int key0 = kb * kT + 64 * x;  // first key column of this half
       const bool band = (a.causal != 0) | (a.window >= 0);
       const bool need_mask = (key0 + 64 > kv_limit) || (band && key0 + 63 > q0) ||
                              (a.window >= 0 && key0 < q0 + kT - 1 - a.window);
@@ -692,12 +732,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dpfree);
       uint32_t w[32];
+      // dS = P o (dP - D); with dropout dP = (dO V^T) Z / q.
+      auto ds_step = [&](auto drop) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float d0 = p[2 * e] * (__uint_as_float(dr[e >> 4][(2 * e) & 31]) - Dr);
-        const float d1 = p[2 * e + 1] * (__uint_as_float(dr[e >> 4][(2 * e + 1) & 31]) - Dr);
-        w[e] = pack_bf16(d0, d1);
-      }
+        for (int e = 0; e < 32; ++e) {
+          float g0 = __uint_as_float(dr[e >> 4][(2 * e) & 31]);
+          float g1 = __uint_as_float(dr[e >> 4][(2 * e + 1) & 31]);
+          if constexpr (decltype(drop)::value) {
+            g0 = (km >> (2 * e)) & 1u ? g0 * a.drop_scale : 0.f;
+            g1 = (km >> (2 * e + 1)) & 1u ? g1 * a.drop_scale : 0.f;
+          }
+          w[e] = pack_bf16(p[2 * e] * (g0 - Dr), p[2 * e + 1] * (g1 - Dr));
+        }
+      };
+      if constexpr (DROP)
+        ds_step(std::true_type{});
+      else
+        ds_step(std::false_type{});
       // dS over the first half of this warpgroup's columns of S_j's buffer
       tmem_st32(tl + C::kColS + 128u * (j & 1) + 64u * x, w);
       tmem_wait_st();
@@ -769,31 +820,31 @@ cudaError_t set_smem_w(Kern k, int bytes, bool (&done)[64]) {
   return cudaSuccess;
 }
 
-template <int HD>
+template <int HD, bool DROP>
 cudaError_t launch_dkdv_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdArgs& a, cudaStream_t stream) {
   static bool done[64] = {};
-  cudaError_t e = set_smem_w(fa_bwd_dkdv_wide_kernel<HD>, KvW<HD>::kSmemBytes, done);
+  cudaError_t e = set_smem_w(fa_bwd_dkdv_wide_kernel<HD, DROP>, KvW<HD>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(a.n_ktiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dkdv_wide_kernel<HD><<<static_cast<unsigned>(grid), kThreads, KvW<HD>::kSmemBytes,
+  fa_bwd_dkdv_wide_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, KvW<HD>::kSmemBytes,
                                 stream>>>(tmQ, tmK, tmV, tmdO, a);
   return cudaGetLastError();
 }
 
-template <int HD>
+template <int HD, bool DROP>
 cudaError_t launch_dq_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdArgs& a,
                         cudaStream_t stream) {
   static bool done[64] = {};
-  cudaError_t e = set_smem_w(fa_bwd_dq_wide_kernel<HD>, QW<HD>::kSmemBytes, done);
+  cudaError_t e = set_smem_w(fa_bwd_dq_wide_kernel<HD, DROP>, QW<HD>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dq_wide_kernel<HD><<<static_cast<unsigned>(grid), kThreads, QW<HD>::kSmemBytes,
+  fa_bwd_dq_wide_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, QW<HD>::kSmemBytes,
                               stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, a);
   return cudaGetLastError();
 }
@@ -804,8 +855,12 @@ cudaError_t launch_bwd_dkdv_wide(int d, const CUtensorMap& tmQ, const CUtensorMa
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                  const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dkdv_w<64>(tmQ, tmK, tmV, tmdO, a, stream);
-    case 128: return launch_dkdv_w<128>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 64:
+      return a.drop_thr ? launch_dkdv_w<64, true>(tmQ, tmK, tmV, tmdO, a, stream)
+                        : launch_dkdv_w<64, false>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 128:
+      return a.drop_thr ? launch_dkdv_w<128, true>(tmQ, tmK, tmV, tmdO, a, stream)
+                        : launch_dkdv_w<128, false>(tmQ, tmK, tmV, tmdO, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -814,8 +869,12 @@ cudaError_t launch_bwd_dq_wide(int d, const CUtensorMap& tmQ, const CUtensorMap&
                                const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                const CUtensorMap& tmdQ, const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dq_w<64>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
-    case 128: return launch_dq_w<128>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 64:
+      return a.drop_thr ? launch_dq_w<64, true>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream)
+                        : launch_dq_w<64, false>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 128:
+      return a.drop_thr ? launch_dq_w<128, true>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream)
+                        : launch_dq_w<128, false>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -34,6 +34,7 @@
 
 #include "kernels.h"
 #include "masks.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -42,8 +43,11 @@ namespace {
 constexpr int kBR = 128;      // query rows per block (MMA M)
 constexpr int kBC = 128;      // keys per block (MMA N of S, K of PV)
 constexpr int kThreads = 384;
-constexpr int kRegsLow = 64;    // warps 0-3 (producer, MMA) after setmaxnreg.dec
-constexpr int kRegsHigh = 216;  // softmax warpgroups after setmaxnreg.inc
+// Registers per thread after setmaxnreg: warps 0-3 (producer, MMA) and the
+// softmax warpgroups.  The dropout variant moves 8 more to the softmax, which
+// also runs the random-number generator.
+template <bool DROP> constexpr int kRegsLow = DROP ? 56 : 64;
+template <bool DROP> constexpr int kRegsHigh = DROP ? 224 : 216;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 8
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -87,7 +91,9 @@ __device__ __forceinline__ void bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int HD>
+// DROP: dropout on P (a separate instantiation, so the kernel without it
+// carries none of its code).
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow<DROP>));
     if (warp == 0 && lane == 0 && T > 0) {
       // ---------------------------------------------------------- producer
       const uint64_t pol_q = policy_evict_first();
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar_drain, 0);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh<DROP>));
     // ------------------------------------------------------------ softmax
     const int x = (warp >> 2) - 1;          // 0: block A (warps 4-7), 1: block B (warps 8-11)
     const int Tn = x == 0 ? TA : TB;        // TB = 0 when there is no block B
@@ -341,7 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float lh_run = 0.f;                     // row sum of P rounded to bf16
     bool ok = true;
     int kb = next_kb(ulo);
+    const uint32_t hh = static_cast<uint32_t>(bh % a.H), bb = static_cast<uint32_t>(b);
     for (int j = 0; j < Tn; ++j) {
+      // Dropout keep bits of this row's 128 keys, drawn while S is computed;
+      // the empty asm keeps the generator from being scheduled among the S
+      // registers below (it would not fit in the register budget there).
+      uint32_t kmask4[4] = {0u, 0u, 0u, 0u};
+      if constexpr (DROP) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          kmask4[c] = keep32(static_cast<uint32_t>(kb * kBC + 32 * c), static_cast<uint32_t>(grow),
+                             hh, bb, a.seed_lo, a.seed_hi, a.drop_thr);
+        asm volatile("" : "+r"(kmask4[0]), "+r"(kmask4[1]), "+r"(kmask4[2]), "+r"(kmask4[3]));
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(x), j & 1, ab))) {
         ok = false;
         break;
@@ -389,13 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bf16 rounding of O.
       const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      // With dropout the product takes P * Z / q; L and the divisor of O stay
+      // the sums of the undropped P.
       float sum_l, sum_h;
-      auto p_tile = [&](auto rounded_sum) {
-        constexpr bool kRounded = decltype(rounded_sum)::value;
+      auto p_tile = [&](auto mode) {
+        constexpr bool kRounded = decltype(mode)::value == 1;
+        constexpr bool kDrop = decltype(mode)::value == 2;
         uint64_t se[2] = {0ull, 0ull}, sh[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
+          const uint32_t kmask = kmask4[c];  // dropout keep bits of the chunk's 32 keys
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float t0, t1;
@@ -403,7 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              scl2, nm2),
                       t0, t1);
             const float p0 = ex2(t0), p1 = ex2(t1);
-            pk[e] = pack_bf16(p0, p1);
+            if constexpr (kDrop) {
+              const float d0 = (kmask >> (2 * e)) & 1u ? p0 * a.drop_scale : 0.f;
+              const float d1 = (kmask >> (2 * e + 1)) & 1u ? p1 * a.drop_scale : 0.f;
+              pk[e] = pack_bf16(d0, d1);
+            } else {
+              pk[e] = pack_bf16(p0, p1);
+            }
             se[e & 1] = f2_add(se[e & 1], f2_pack(p0, p1));
             if constexpr (kRounded) sh[e & 1] = f2_add(sh[e & 1], bf16x2_to_f2(pk[e]));
           }
@@ -419,10 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           sum_h = u0 + u1;
         }
       };
-      if (crossing)
-        p_tile(std::true_type{});
+      if constexpr (DROP)
+        p_tile(std::integral_constant<int, 2>{});
+      else if (crossing)
+        p_tile(std::integral_constant<int, 1>{});
       else
-        p_tile(std::false_type{});
+        p_tile(std::integral_constant<int, 0>{});
       l_run = l_run * alpha + sum_l;
       lh_run = lh_run * alpha + sum_h;
       m_run = m_new;
@@ -504,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD>
+template <int HD, bool DROP>
 cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          const CUtensorMap& tmO, const FwdArgs& a, cudaStream_t stream) {
   using C = Cfg<HD>;
@@ -516,10 +546,11 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
     // The register split (setmaxnreg) must fit in what the launch provides,
     // or the increasing warpgroups would wait for registers forever.
     cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, fa_fwd_kernel<HD>);
+    e = cudaFuncGetAttributes(&fattr, fa_fwd_kernel<HD, DROP>);
     if (e != cudaSuccess) return e;
-    if (fattr.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(fa_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (fattr.numRegs * kThreads < 128 * kRegsLow<DROP> + 256 * kRegsHigh<DROP>)
+      return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(fa_fwd_kernel<HD, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -527,7 +558,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   const long long grid = static_cast<long long>((a.n_qtiles + 1) / 2) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_kernel<HD><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
+  fa_fwd_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
                                                                                     tmO, a);
   return cudaGetLastError();
 }
@@ -538,8 +569,12 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_fwd_t<64>(tmQ, tmK, tmV, tmO, a, stream);
-    case 128: return launch_fwd_t<128>(tmQ, tmK, tmV, tmO, a, stream);
+    case 64:
+      return a.drop_thr ? launch_fwd_t<64, true>(tmQ, tmK, tmV, tmO, a, stream)
+                        : launch_fwd_t<64, false>(tmQ, tmK, tmV, tmO, a, stream);
+    case 128:
+      return a.drop_thr ? launch_fwd_t<128, true>(tmQ, tmK, tmV, tmO, a, stream)
+                        : launch_fwd_t<128, false>(tmQ, tmK, tmV, tmO, a, stream);
     case 256: return launch_fwd_d256(tmQ, tmK, tmV, tmO, a, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -18,6 +18,9 @@ struct FwdArgs {
   int window;           // < 0: none; w >= 0: keys i - w <= j <= i only
   const uint8_t* bmask; // block mask [nb, nb] (query block, key block) or nullptr
   int nb;               // ceil(N / 128)
+  uint32_t drop_thr;    // dropout: 0 = none, else floor(p * 65536)
+  uint32_t seed_lo, seed_hi;
+  float drop_scale;     // 65536 / (65536 - drop_thr)
 };
 
 // Forward: grid = n_qtiles * BH CTAs.
@@ -57,6 +60,9 @@ struct BwdArgs {
   int window;           // < 0: none; w >= 0: keys i - w <= j <= i only
   const uint8_t* bmask; // block mask [nb, nb] (query block, key block) or nullptr
   int nb;               // ceil(N / 128)
+  uint32_t drop_thr;    // dropout: 0 = none, else floor(p * 65536)
+  uint32_t seed_lo, seed_hi;
+  float drop_scale;     // 65536 / (65536 - drop_thr)
 };
 
 // Query rows per step of the dK/dV kernel (the box height of its Q and dO

@@ -40,6 +40,10 @@ def load_library():
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_kvlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
     lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp]
+    u64 = ctypes.c_uint64
+    lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, f, u64, vp]
+    lib.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i,
+                                   vp, f, u64, vp, sz, vp]
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
@@ -55,6 +59,7 @@ def load_library():
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_fwd_masked", "fa_bwd", "fa_bwd_masked",
+               "fa_fwd_dropout", "fa_bwd_dropout",
                "fa_bwd_prepare", "fa_bwd_dkdv",
                "fa_bwd_dq", "fa_check_error", "fa_selftest_stalled_wait"):
         getattr(lib, fn).restype = ctypes.c_int
@@ -123,6 +128,29 @@ def fa_fwd_masked(q, k, v, o, L, scale, causal, kv_len, window, block_mask, stre
     _check(load_library().fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d,
                                         float(scale), int(bool(causal)), _ptr(kv_len), int(window),
                                         _ptr(block_mask), _stream(stream, q)), "fa_fwd_masked")
+
+
+def fa_fwd_dropout(q, k, v, o, L, scale, causal, kv_len, window, block_mask, dropout_p, seed,
+                   stream=None):
+    """fa_fwd_dropout: the masked forward with dropout (p in [0, 1), 64-bit seed)."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d,
+                                         float(scale), int(bool(causal)), _ptr(kv_len),
+                                         int(window), _ptr(block_mask), float(dropout_p),
+                                         int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream, q)),
+           "fa_fwd_dropout")
+
+
+def fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
+                   dropout_p, seed, workspace, stream=None):
+    """fa_bwd_dropout on torch tensors (same masks, p and seed as the forward)."""
+    B, H, N, d = _shape(q)
+    _check(load_library().fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
+                                         _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                         int(bool(causal)), _ptr(kv_len), int(window),
+                                         _ptr(block_mask), float(dropout_p),
+                                         int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(workspace),
+                                         workspace.numel(), _stream(stream, q)), "fa_bwd_dropout")
 
 
 def fa_bwd_workspace_bytes(B, H, N, d):
@@ -213,7 +241,7 @@ def _expect_mask(block_mask, N):
 
 
 def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=None, stream=None,
-                  window=-1, block_mask=None):
+                  window=-1, block_mask=None, dropout_p=0.0, seed=0):
     """Exact attention forward.  Returns (O bf16 [B,H,N,d], L fp32 [B,H,N]).
 
     window (int, -1 = none) and block_mask (CUDA uint8 [ceil(N/128)]^2 or None)
@@ -230,7 +258,11 @@ def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if kv_len is not None:
         _expect(kv_len, "kv_len", torch.int32, (B,))
-    if window >= 0 or block_mask is not None:
+    if dropout_p > 0.0:
+        _expect_mask(block_mask, N)
+        fa_fwd_dropout(q, k, v, out, lse, scale, causal, kv_len, window, block_mask, dropout_p,
+                       seed, stream)
+    elif window >= 0 or block_mask is not None:
         _expect_mask(block_mask, N)
         fa_fwd_masked(q, k, v, out, lse, scale, causal, kv_len, window, block_mask, stream)
     else:
@@ -239,7 +271,7 @@ def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=
 
 
 def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, workspace=None,
-                  stream=None, window=-1, block_mask=None):
+                  stream=None, window=-1, block_mask=None, dropout_p=0.0, seed=0):
     """Exact attention backward.  Returns (dQ, dK, dV), bf16 [B,H,N,d]."""
     import torch
     B, H, N, d = _shape(q)
@@ -254,7 +286,11 @@ def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, work
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    if window >= 0 or block_mask is not None:
+    if dropout_p > 0.0:
+        _expect_mask(block_mask, N)
+        fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
+                       dropout_p, seed, workspace, stream)
+    elif window >= 0 or block_mask is not None:
         _expect_mask(block_mask, N)
         fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
                       workspace, stream)

@@ -106,6 +106,28 @@ fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, fl
                         int window, const uint8_t* block_mask, fa_stream_t stream);
 
 /*
+ * Forward with dropout on the attention weights (the study notes list dropout
+ * among the steps fused into the kernel, section "Kernel融合"), plus every
+ * mask term of fa_fwd_masked:
+ *   dropout_p     : drop probability, 0 <= p < 1 (0 = no dropout).  Weight
+ *                   P_ij is kept and scaled by 1/q, or replaced by 0; O uses
+ *                   the dropped weights, L stays the logsumexp of the scores.
+ *   dropout_seed  : 64-bit key of the generator.
+ * Decisions: Philox4x32-10 (Salmon et al., SC'11) at counter (j / 8, i, h, b)
+ * with key (seed low word, seed high word); its 128 bits are eight 16-bit
+ * values, value j % 8 (low half of word (j % 8) / 2 first) deciding key j:
+ * kept iff value >= thr = floor(p * 65536), so q = (65536 - thr) / 65536 and
+ * the scale is exactly 1/q.  The same (seed, p) gives the same decisions in
+ * fa_bwd_dropout, which must be called with them.
+ * Errors: p outside [0, 1) gives FA_ERR_INVALID_ARG; p > 0 with d = 256 gives
+ * FA_ERR_UNSUPPORTED; otherwise as fa_fwd_masked.
+ */
+fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                         int window, const uint8_t* block_mask, float dropout_p,
+                         uint64_t dropout_seed, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: the fp32 [B, H, N] row terms
  * D_i = sum_c dO_ic O_ic, rounded up to 256 bytes.  Returns 0 for invalid
  * sizes.
@@ -140,6 +162,19 @@ fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void*
                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
                         int window, const uint8_t* block_mask, void* workspace,
                         size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_bwd_masked with dropout: gradients of sum(O * dO) for the O of
+ * fa_fwd_dropout with the same masks, dropout_p and dropout_seed (the
+ * decisions are regenerated, never stored).  dV = (P Z / q)^T dO and
+ * dS = P o ((dO V^T) Z / q - D), D_i = sum_c dO_ic O_ic.
+ */
+fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t* kv_len,
+                         int window, const uint8_t* block_mask, float dropout_p,
+                         uint64_t dropout_seed, void* workspace, size_t workspace_bytes,
+                         fa_stream_t stream);
 
 /*
  * The three stages fa_bwd enqueues, for callers that want to schedule or time

@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_dkdv",
               "fa_bwd_dq", "fa_bwd_workspace_bytes", "fa_check_error", "fa_status_string",
-              "fa_selftest_stalled_wait", "fa_bwd_noalloc", "fa_fwd_masked", "fa_bwd_masked"):
+              "fa_selftest_stalled_wait", "fa_bwd_noalloc", "fa_fwd_masked", "fa_bwd_masked",
+              "fa_fwd_dropout", "fa_bwd_dropout"):
         assert n in names
 
 
@@ -119,3 +120,17 @@ def test_masked_entry_points_validate_the_mask_terms(lib):
                              null) == 1
     assert lib.fa_bwd_masked(*([fake] * 9), 1, 1, 256, 64, f(0.1), 1, null, 4, null, fake, 16,
                              null) == 1          # short workspace
+
+
+def test_dropout_entry_points_validate_the_probability(lib):
+    fake, null, f = ctypes.c_void_p(0x10000), ctypes.c_void_p(0), ctypes.c_float
+    u64 = ctypes.c_uint64
+    fwd = lambda d, p: lib.fa_fwd_dropout(*([fake] * 5), 1, 1, 256, d, f(0.1), 1, null, -1, null,
+                                           f(p), u64(7), null)
+    bwd = lambda d, p: lib.fa_bwd_dropout(*([fake] * 9), 1, 1, 256, d, f(0.1), 1, null, -1, null,
+                                           f(p), u64(7), fake, 1 << 20, null)
+    for call in (fwd, bwd):
+        assert call(64, -0.1) == 1
+        assert call(64, 1.0) == 1
+        assert call(64, float("nan")) == 1
+        assert call(256, 0.1) == 2      # dropout on the d = 256 kernels
