@@ -12,7 +12,7 @@ dQ); non-causal P = B*H*N^2, causal P = B*H*N(N+1)/2.  The dQ kernel recomputes
 QK^T and dP a second time; those 4*d*P are not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--mask dense|causal|window:W|blocksparse] [--dropout P]
+                    [--mask dense|causal|window:W|blocksparse] [--dropout P] [--configs]
 
 --mask measures one variant instead (same inputs; one step = fa_fwd_dropout +
 fa_bwd_dropout with that mask): dense or causal attention; window:W keeps keys
@@ -20,6 +20,12 @@ i - W .. i of each query; blocksparse keeps, over 128 x 128 blocks, a band of
 three blocks around the diagonal plus the first four key blocks (a
 local + global layout).  --dropout P adds dropout with probability P (seed
 fixed).  FLOPs count only the pairs the mask keeps.
+
+--configs times the forward and the backward alone on every workload of the
+configuration list (tiny; BERT-large-shaped B=16 H=16 N=512 d=64 with key
+lengths uniform in [256, 512]; GPT-2-shaped B=8 H=12 N=1024 d=64 causal; the
+long-sequence workload; the sweep N = 512..16384, B = 16384/N, H = 2048/d,
+d = 64, 128, 256, causal off and on) and prints one JSON line per workload.
 
 Under torchrun each rank runs the same workload on its own GPU (independent
 replicas, no collective on the data path); rank 0 prints one JSON line.
@@ -408,6 +414,85 @@ def run_masked(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- all workloads
+
+def config_list():
+    """(name, B, H, N, d, causal, kv_range, seed) of every workload."""
+    out = [("tiny", 1, 2, 128, 64, c, None, 1000) for c in (0, 1)]
+    out.append(("bert-large-shaped", 16, 16, 512, 64, 0, (256, 512), 1001))
+    out.append(("gpt2-shaped", 8, 12, 1024, 64, 1, None, 1002))
+    out += [("long", 1, 16, 16384, 128, c, None, 1003) for c in (0, 1)]
+    for d in (64, 128, 256):
+        for n in (512, 1024, 2048, 4096, 8192, 16384):
+            for c in (0, 1):
+                out.append(("sweep", 16384 // n, 2048 // d, n, d, c, None, 1004))
+    return out
+
+
+def run_configs(args):
+    import numpy as np
+    import torch
+    from exact_io_aware_40_gb300 import build as fab, fa, inputs
+
+    fab.build()
+    fa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_uuid = dev.index
+    for (name, b, h, n, d, causal, kv_range, seed) in config_list():
+        gen = torch.Generator(device="cpu").manual_seed(seed)
+        q, k, v, do = (torch.randn(b, h, n, d, generator=gen).to(torch.bfloat16).to(dev)
+                       for _ in range(4))
+        kv = None
+        if kv_range is not None:
+            lens = inputs.kv_lengths(seed, b, *kv_range)
+            kv = torch.from_numpy(lens).to(dev)
+            i = np.arange(n)
+            vis = (i + 1) if causal else np.full(n, n)
+            pairs_ = h * int(sum(np.minimum(vis, min(int(x), n)).sum() for x in lens))
+        else:
+            pairs_ = b * h * (n * (n + 1) // 2 if causal else n * n)
+        scale = 1.0 / math.sqrt(d)
+        o = torch.empty_like(q)
+        L = torch.empty((b, h, n), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(b, h, n, d), dtype=torch.uint8, device=dev)
+        fwd = lambda: fa.fa_fwd_kvlen(q, k, v, o, L, scale, causal, kv)
+        bwd = lambda: fa.fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv, ws)
+        for _ in range(max(3, args.warmup)):
+            fwd()
+            bwd()
+        fa.fa_check_error()
+        reps = max(5, min(args.steps, 20))
+        times = {}
+        sampler = ClockSampler(gpu_uuid)
+        with sampler:
+            for nm, fn in (("fwd", fwd), ("bwd", bwd)):
+                torch.cuda.synchronize()
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record()
+                for _ in range(reps):
+                    fn()
+                s1.record()
+                torch.cuda.synchronize()
+                times[nm] = s0.elapsed_time(s1) / reps
+        fa.fa_check_error()
+        f_t = 4 * d * pairs_ / (times["fwd"] * 1e-3) / 1e12
+        b_t = 10 * d * pairs_ / (times["bwd"] * 1e-3) / 1e12
+        print(json.dumps({
+            "workload": name, "B": b, "H": h, "N": n, "d": d, "causal": causal,
+            "kv_len": None if kv_range is None else "U[%d,%d]" % kv_range,
+            "visible_pairs": pairs_, "fwd_ms": times["fwd"], "bwd_ms": times["bwd"],
+            "fwd_tflops": f_t, "bwd_tflops": b_t, "fwd_frac_of_burst": f_t / burst,
+            "bwd_frac_of_burst": b_t / burst, "peak": burst, "peak_source": peak_src,
+            "l2": "warm (inputs of the small workloads fit in L2)",
+            "clocks": sampler.summary()}), flush=True)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world):
@@ -595,6 +680,8 @@ def main():
                     help="skip timing the oracle on the host cores")
     ap.add_argument("--mask", default=None,
                     help="measure one variant: dense, causal, window:W or blocksparse")
+    ap.add_argument("--configs", action="store_true",
+                    help="time forward and backward on every workload, one JSON line each")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout probability of the --mask variant (default 0)")
     ap.add_argument("--heads", type=int, default=16,
@@ -634,7 +721,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
     try:
-        if args.mask:
+        if args.configs:
+            if rank == 0:
+                run_configs(args)
+        elif args.mask:
             run_masked(args, rank, world)
         else:
             run_ours(args, rank, world)

@@ -1,6 +1,8 @@
 """Shared helpers of the GPU parity tests: seeded inputs on the device, the
 same inputs widened to fp64 for the oracle, and the error measures."""
+import json
 import math
+import os
 
 import numpy as np
 
@@ -59,3 +61,17 @@ def err_rel(g, g_ref):
     if den == 0.0:
         return num
     return num / den
+
+
+def report(kind, case, causal, **errs):
+    """Append the measured errors of one check as a JSON line to the file named
+    by FA_PARITY_REPORT (no-op when unset); used to tabulate parity results."""
+    path = os.environ.get("FA_PARITY_REPORT")
+    if not path:
+        return
+    rec = {"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "kind": kind,
+           "B": case.B, "H": case.H, "N": case.N, "d": case.d, "causal": int(bool(causal)),
+           "kv_len": None if case.kv_len is None else [int(x) for x in case.kv_len]}
+    rec.update({k: float(v) for k, v in errs.items()})
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")

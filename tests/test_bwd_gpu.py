@@ -35,6 +35,7 @@ def check_full(case, causal):
     ref = oracle.attn_bwd(case.f64["Q"], case.f64["K"], case.f64["V"], case.f64["dO"],
                           case.scale, causal, kv_len=case.kv_len)
     errs = [H.err_rel(g, r) for g, r in zip(got, ref)]
+    H.report("bwd", case, causal, err_dQ=errs[0], err_dK=errs[1], err_dV=errs[2])
     for name, e in zip(("dQ", "dK", "dV"), errs):
         assert e <= H.TOL_GRAD_REL, (name, e)
     return errs
@@ -42,6 +43,7 @@ def check_full(case, causal):
 
 def check_sampled(case, causal, heads, rows, cols):
     dq, dk, dv = run_bwd(case, causal)
+    worst = {"dQ": 0.0, "dK": 0.0, "dV": 0.0}
     for (b, h) in heads:
         qh, kh, vh, doh = (case.f64[n][b, h] for n in ("Q", "K", "V", "dO"))
         ln = case.length(b)
@@ -51,7 +53,10 @@ def check_sampled(case, causal, heads, rows, cols):
         for name, g, r in (("dQ", dq[b, h, rows], dq_ref), ("dK", dk[b, h, cols], dk_ref),
                            ("dV", dv[b, h, cols], dv_ref)):
             e = H.err_rel(g, r)
+            worst[name] = max(worst[name], e)
             assert e <= H.TOL_GRAD_REL, (name, b, h, e)
+    H.report("bwd_sampled", case, causal, err_dQ=worst["dQ"], err_dK=worst["dK"],
+             err_dV=worst["dV"])
 
 
 @pytest.mark.parametrize("causal", [False, True])

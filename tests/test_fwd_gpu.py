@@ -37,6 +37,7 @@ def check_full(case, causal):
     o_ref, L_ref = oracle.attn_fwd(case.f64["Q"], case.f64["K"], case.f64["V"], case.scale,
                                    causal, kv_len=case.kv_len)
     eo, el = H.err_o(o, o_ref), H.err_l(L, L_ref)
+    H.report("fwd", case, causal, err_O=eo, err_L=el)
     assert eo <= H.TOL_O_ABS, ("O", eo)
     assert el <= H.TOL_L_ABS, ("L", el)
     return eo, el
@@ -50,6 +51,7 @@ def check_rows(case, causal, heads, rows):
         o_ref, L_ref = oracle.fwd_rows(qh, kh, vh, case.scale, causal, case.length(b), rows)
         worst_o = max(worst_o, H.err_o(o[b, h, rows], o_ref))
         worst_l = max(worst_l, H.err_l(L[b, h, rows], L_ref))
+    H.report("fwd_sampled", case, causal, err_O=worst_o, err_L=worst_l)
     assert worst_o <= H.TOL_O_ABS, ("O", worst_o)
     assert worst_l <= H.TOL_L_ABS, ("L", worst_l)
 
