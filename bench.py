@@ -55,10 +55,10 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
 # launches), valid only while the kernel source hashes to the recorded digest.
 # Capture: H=8 (same kernels, half the heads, inputs still larger than L2),
-# 135.3 MB read + 32.7 MB written (causal 0) and 135.3 + 27.6 MB (causal 1);
+# 135.3 MB read + 32.2 MB written (causal 0) and 135.4 + 27.8 MB (causal 1);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "26021beb28b7713a4d6e20c47160a78942bce904f22a3522a0a7f17cb3bbf8bd",
-                    "bytes_per_launch": 2 * (168.0e6 + 162.9e6) / 2}
+BWD_DKDV_TRAFFIC = {"sha256": "a3eb85a39990c4f660320d7f2c88263dff914aa0dc39d8b973cd7bbd9393c181",
+                    "bytes_per_launch": 2 * (167.6e6 + 163.2e6) / 2}
 
 
 def pairs(causal, b=None, h=None, n=None):
