@@ -13,6 +13,7 @@ QK^T and dP a second time; those 4*d*P are not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--mask dense|causal|window:W|blocksparse] [--dropout P] [--configs]
+                    [--fp8]
 
 --mask measures one variant instead (same inputs; one step = fa_fwd_dropout +
 fa_bwd_dropout with that mask): dense or causal attention; window:W keeps keys
@@ -20,6 +21,10 @@ i - W .. i of each query; blocksparse keeps, over 128 x 128 blocks, a band of
 three blocks around the diagonal plus the first four key blocks (a
 local + global layout).  --dropout P adds dropout with probability P (seed
 fixed).  FLOPs count only the pairs the mask keeps.
+
+--fp8 times the e4m3 forward (fa_fwd_fp8, d = 128) on the long workload: the
+same N(0,1) draws rounded to e4m3 codes (dequantisation factors 1), causal 0
+and 1; one step = the two forward calls, each with its V transpose.
 
 --configs times the forward and the backward alone on every workload of the
 configuration list (tiny; BERT-large-shaped B=16 H=16 N=512 d=64 with key
@@ -414,6 +419,131 @@ def run_masked(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- e4m3 forward
+
+def run_fp8(args, rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from exact_io_aware_40_gb300 import build as fab, fa, inputs
+
+    fab.build()
+    fa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    scale = 1.0 / math.sqrt(D)
+    host = {n: torch.from_numpy(inputs.normal_e4m3_bits(SEED, inputs.STREAM[n], (B, H, N, D)))
+            .pin_memory() for n in ("Q", "K", "V")}
+    q, k, v = (host[n].to(dev) for n in ("Q", "K", "V"))
+    out = {c: (torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev),
+               torch.empty((B, H, N), dtype=torch.float32, device=dev)) for c in (0, 1)}
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step(ev=None):
+        for c in (0, 1):
+            if ev is not None:
+                ev[c][0].record(stream)
+            fa.fa_fwd_fp8(q, k, v, out[c][0], out[c][1], scale, 1.0, 1.0, 1.0, c, None, ws,
+                          stream=sp)
+            if ev is not None:
+                ev[c][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    fa.fa_check_error(sp)
+    torch.cuda.synchronize()
+    barrier()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in (0, 1)]
+           for _ in range(args.steps)]
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_uuid = dev.index
+    sampler = ClockSampler(gpu_uuid)
+    with sampler:
+        torch.cuda.synchronize()
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s_ in range(args.steps):
+            step(evs[s_])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    fa.fa_check_error(sp)
+    ms_step = t0.elapsed_time(t1) / args.steps
+    per_c = {c: sum(e[c][0].elapsed_time(e[c][1]) for e in evs) / args.steps for c in (0, 1)}
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    flops = sum(4 * D * pairs(c) for c in (0, 1))
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    host_out = {c: (torch.empty(out[c][0].shape, dtype=torch.bfloat16).pin_memory(),
+                    torch.empty(out[c][1].shape, dtype=torch.float32).pin_memory()) for c in (0, 1)}
+    h2d = sum(host[n].numel() for n in ("Q", "K", "V"))
+    d2h = sum(t.numel() * t.element_size() for c in (0, 1) for t in host_out[c])
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for dst, nm in ((q, "Q"), (k, "K"), (v, "V")):
+            dst.copy_(host[nm], non_blocking=True)
+        step()
+        for c in (0, 1):
+            host_out[c][0].copy_(out[c][0], non_blocking=True)
+            host_out[c][1].copy_(out[c][1], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_check_error(sp)
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    # e4m3 peak: the measured bf16 figure times the nominal e4m3 / bf16 ratio (2)
+    peak = 2.0 * float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = 4 * D * pairs(0) / (per_c[0] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": "long-sequence attention B=%d H=%d N=%d d=%d, e4m3 Q/K/V, bf16 O, "
+                               "forward, causal=0 and causal=1" % (B, H, N, D),
+                   "B": B, "H": H, "N": N, "d": D, "causal": [0, 1], "passes": "fwd",
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (32 MiB per e4m3 tensor x 3 + V^T) -- no flush"},
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd_fp8 (causal=0 launch, V transpose included)",
+                     "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "traffic": None,
+                     "peak_source": "2 x bf16_tflops_sustained of %s peaks (nominal e4m3/bf16 "
+                                    "ratio)" % peak_src,
+                     "frac_of_burst_peak": achieved / burst},
+        "cpu_baseline": None,
+        "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": 4 * args.steps,
+        "clocks": sampler.summary(),
+        "per_pass": {"fwd_ms": {str(c): per_c[c] for c in (0, 1)},
+                     "fwd_tflops": {str(c): 4 * D * pairs(c) / (per_c[c] * 1e-3) / 1e12
+                                    for c in (0, 1)}},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- all workloads
 
 def config_list():
@@ -680,6 +810,8 @@ def main():
                     help="skip timing the oracle on the host cores")
     ap.add_argument("--mask", default=None,
                     help="measure one variant: dense, causal, window:W or blocksparse")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the e4m3 forward on the long workload")
     ap.add_argument("--configs", action="store_true",
                     help="time forward and backward on every workload, one JSON line each")
     ap.add_argument("--dropout", type=float, default=0.0,
@@ -721,7 +853,9 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
     try:
-        if args.configs:
+        if args.fp8:
+            run_fp8(args, rank, world)
+        elif args.configs:
             if rank == 0:
                 run_configs(args)
         elif args.mask:

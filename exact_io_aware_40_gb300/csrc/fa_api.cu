@@ -81,6 +81,23 @@ fa_status map_bf16(EncodeTiledFn enc, CUtensorMap* m, const void* base, int d,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// Tensor map over a one-byte [BH, rows, inner] tensor, seen as 3-D (inner,
+// rows, BH) with a (128, box_rows, 1) box and 128-byte swizzle (one box row is
+// one 128-byte atom).  Out-of-range elements read as zero.
+fa_status map_u8(EncodeTiledFn enc, CUtensorMap* m, const void* base, int inner, int rows,
+                 int BH, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                           static_cast<cuuint64_t>(inner) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_common(int B, int H, int N, int d, float scale) {
@@ -214,6 +231,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.seed_lo = drop.seed_lo;
   a.seed_hi = drop.seed_hi;
   a.drop_scale = drop.scale;
+  a.out_scale = 1.f;
   if (fa::launch_fwd(d, tq, tk, tv, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -247,6 +265,62 @@ fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, f
                          uint64_t dropout_seed, fa_stream_t stream) {
   return fwd_impl(Q, K, V, O, L, B, H, N, d, scale, causal, kv_len, window, block_mask, dropout_p,
                   dropout_seed, stream);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d != 128) return 0;
+  const size_t npad = (static_cast<size_t>(N) + 15) / 16 * 16;
+  return round256(static_cast<size_t>(B) * H * d * npad);
+}
+
+fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                     int H, int N, int d, float scale, float descale_q, float descale_k,
+                     float descale_v, int causal, const int32_t* kv_len, void* workspace,
+                     size_t workspace_bytes, fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !L || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  for (float f : {descale_q, descale_k, descale_v})
+    if (!std::isfinite(f) || !(f > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+      !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_fwd_fp8_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  const float prod = scale * descale_q * descale_k;
+  if (!std::isfinite(prod) || !(prod > 0.f)) return FA_ERR_INVALID_ARG;
+  int dev;
+  if ((st = current_device(&dev)) != FA_OK) return st;
+  int* err;
+  if ((st = error_word(dev, &err)) != FA_OK) return st;
+  EncodeTiledFn enc;
+  if ((st = encoder(&enc)) != FA_OK) return st;
+  const int BH = B * H;
+  const int npad = (N + 15) / 16 * 16;
+  CUtensorMap tq, tk, tvt, to;
+  if ((st = map_u8(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_u8(enc, &tk, K, d, N, BH, 128)) != FA_OK) return st;
+  if ((st = map_u8(enc, &tvt, workspace, npad, d, BH, 128)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &to, O, d, N, BH, 128)) != FA_OK) return st;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.L = L;
+  a.kv_len = kv_len;
+  a.err = err;
+  a.H = H;
+  a.N = N;
+  a.BH = BH;
+  a.n_qtiles = (N + 127) / 128;
+  a.scale_log2 = prod * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.window = -1;
+  a.nb = a.n_qtiles;
+  a.drop_scale = 1.f;
+  a.out_scale = descale_v;
+  if (fa::launch_transpose_v8(V, workspace, BH, N, npad, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (fa::launch_fwd_fp8(tq, tk, tvt, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -21,6 +21,7 @@ struct FwdArgs {
   uint32_t drop_thr;    // dropout: 0 = none, else floor(p * 65536)
   uint32_t seed_lo, seed_hi;
   float drop_scale;     // 65536 / (65536 - drop_thr)
+  float out_scale;      // factor applied to O (e4m3 forward: V's dequantisation factor)
 };
 
 // Forward: grid = n_qtiles * BH CTAs.
@@ -34,6 +35,15 @@ cudaError_t launch_fwd_d256(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                             cudaStream_t stream);
 inline int fwd_kv_rows(int d) { return d == 256 ? 64 : 128; }
+
+// e4m3 forward, d = 128 (fa_fwd_fp8.cu): V [BH, N, 128] -> V^T [BH, 128,
+// Npad] (Npad = N rounded up to 16, zero-filled), then the forward with Q, K
+// maps over uint8 [BH, N, 128] (128 x 128 boxes), the V^T map over uint8
+// [BH, 128, Npad] (128 x 128 boxes) and the bf16 O map of fa_fwd.
+cudaError_t launch_transpose_v8(const void* V, void* Vt, int BH, int N, int Npad,
+                                cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmVt,
+                           const CUtensorMap& tmO, const FwdArgs& a, cudaStream_t stream);
 
 struct BwdPreArgs {
   const uint16_t* O;    // bf16 [BH, N, d]

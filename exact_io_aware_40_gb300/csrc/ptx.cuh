@@ -4,6 +4,7 @@
 // (8.7+) descriptions of these instructions; nothing here is generated code.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace fa {
@@ -212,6 +213,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit floating-point operands
+// (kind::f8f6f4; formats in the instruction descriptor), fp32 accumulate.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when all previously issued tcgen05 async ops of this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -292,6 +304,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0 in
+// bits 7-9 and 10-12), fp32 accumulate (bits 4-5 = 1), both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- math helpers
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -321,6 +339,22 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // The two bf16 halves of a packed word, widened (exactly) to an fp32 pair.
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Two fp32 values to e4m3 (round to nearest even, saturating at +-448):
+// lo -> bits 0-7, hi -> bits 8-15.
+__device__ __forceinline__ uint32_t pack_e4m3(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The two e4m3 values of the low 16 bits of w, widened (exactly) to fp32.
+__device__ __forceinline__ void unpack_e4m3(uint32_t w, float& lo, float& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(w)));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  lo = __low2float(h);
+  hi = __high2float(h);
 }
 
 // Packs two fp32 values into bf16x2 (round to nearest even): lo -> bits 0-15.

@@ -46,6 +46,9 @@ def load_library():
                                    vp, f, u64, vp, sz, vp]
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_bytes.restype = sz
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, f, f, i, vp, vp, sz, vp]
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.fa_bwd_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp,
                                   vp, sz, vp]
@@ -59,7 +62,7 @@ def load_library():
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     for fn in ("fa_fwd", "fa_fwd_kvlen", "fa_fwd_masked", "fa_bwd", "fa_bwd_masked",
-               "fa_fwd_dropout", "fa_bwd_dropout",
+               "fa_fwd_dropout", "fa_bwd_dropout", "fa_fwd_fp8",
                "fa_bwd_prepare", "fa_bwd_dkdv",
                "fa_bwd_dq", "fa_check_error", "fa_selftest_stalled_wait"):
         getattr(lib, fn).restype = ctypes.c_int
@@ -151,6 +154,21 @@ def fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window,
                                          _ptr(block_mask), float(dropout_p),
                                          int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(workspace),
                                          workspace.numel(), _stream(stream, q)), "fa_bwd_dropout")
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, N, d):
+    return int(load_library().fa_fwd_fp8_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_fp8(q8, k8, v8, o, L, scale, descale_q, descale_k, descale_v, causal, kv_len,
+               workspace, stream=None):
+    """fa_fwd_fp8: q8/k8/v8 are CUDA uint8 tensors of e4m3 codes [B,H,N,d]; O bf16."""
+    B, H, N, d = _shape(q8)
+    _check(load_library().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(o), _ptr(L), B, H, N, d,
+                                     float(scale), float(descale_q), float(descale_k),
+                                     float(descale_v), int(bool(causal)), _ptr(kv_len),
+                                     _ptr(workspace), workspace.numel(), _stream(stream, q8)),
+           "fa_fwd_fp8")
 
 
 def fa_bwd_workspace_bytes(B, H, N, d):

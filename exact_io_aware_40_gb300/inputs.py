@@ -86,6 +86,41 @@ def normal_bf16_bits(seed, stream, shape):
     return f32_to_bf16_bits(normal_f64(seed, stream, n).astype(np.float32)).reshape(shape)
 
 
+def e4m3_bits_to_f64(bits):
+    """Exact values of e4m3 codes (sign, 4 exponent bits with bias 7, 3 mantissa
+    bits; exponent 0 is subnormal; 0x7F/0xFF are NaN, no infinities)."""
+    c = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return s * v
+
+
+_E4M3_POS = e4m3_bits_to_f64(np.arange(0x7F, dtype=np.uint8))  # codes 0 .. 0x7E, ascending
+
+
+def f32_to_e4m3_bits(x):
+    """Round values to e4m3 codes: nearest, ties to the even code, saturating at
+    +-448 (the largest finite value)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = np.abs(a - _E4M3_POS[lo])
+    d_hi = np.abs(_E4M3_POS[hi] - a)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def normal_e4m3_bits(seed, stream, shape):
+    """iid N(0,1) values rounded fp64 -> e4m3 codes (uint8)."""
+    n = int(np.prod(shape))
+    return f32_to_e4m3_bits(normal_f64(seed, stream, n)).reshape(shape)
+
+
 def kv_lengths(seed, B, lo, hi):
     """Per-sequence key lengths, uniform integers in [lo, hi] (int32 [B])."""
     u = uint64_stream(seed, STREAM["kv_len"], B)

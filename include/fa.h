@@ -128,6 +128,28 @@ fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, f
                          uint64_t dropout_seed, fa_stream_t stream);
 
 /*
+ * Forward with 8-bit floating-point inputs, the FP8 direction the pages name
+ * for the method (bxzpzcl.cn article, section "量化技术深度融合").
+ *   Q, K, V   in : e4m3 codes (1 byte: sign, 4 exponent bits with bias 7, 3
+ *                  mantissa bits; no infinities, 0x7F/0xFF are NaN, largest
+ *                  finite 448), contiguous [B, H, N, d], DEVICE, 16-byte aligned
+ *   descale_q, descale_k, descale_v : per-tensor factors, finite and > 0; the
+ *                  values are factor * code
+ *   O        out : bf16 [B, H, N, d] = softmax(scale * (dq Q)(dk K)^T + mask) (dv V)
+ *   L        out : fp32 [B, H, N], as fa_fwd
+ *   workspace    : DEVICE, >= fa_fwd_fp8_workspace_bytes(B, H, N, d) bytes,
+ *                  256-byte aligned; receives a transposed copy of V
+ * The products run in e4m3 with fp32 accumulation; P enters the PV product
+ * rounded to e4m3 and O is divided by the sum of those rounded weights.
+ * d must be 128 (FA_ERR_UNSUPPORTED otherwise).  Masks: causal and kv_len.
+ */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                     int H, int N, int d, float scale, float descale_q, float descale_k,
+                     float descale_v, int causal, const int32_t* kv_len, void* workspace,
+                     size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: the fp32 [B, H, N] row terms
  * D_i = sum_c dO_ic O_ic, rounded up to 256 bytes.  Returns 0 for invalid
  * sizes.

@@ -35,7 +35,7 @@ def test_header_declares_the_entry_points():
     for n in ("fa_fwd", "fa_fwd_kvlen", "fa_bwd", "fa_bwd_prepare", "fa_bwd_dkdv",
               "fa_bwd_dq", "fa_bwd_workspace_bytes", "fa_check_error", "fa_status_string",
               "fa_selftest_stalled_wait", "fa_bwd_noalloc", "fa_fwd_masked", "fa_bwd_masked",
-              "fa_fwd_dropout", "fa_bwd_dropout"):
+              "fa_fwd_dropout", "fa_bwd_dropout", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes"):
         assert n in names
 
 
@@ -134,3 +134,16 @@ def test_dropout_entry_points_validate_the_probability(lib):
         assert call(64, 1.0) == 1
         assert call(64, float("nan")) == 1
         assert call(256, 0.1) == 2      # dropout on the d = 256 kernels
+
+
+def test_fp8_entry_point_validates_on_the_host(lib):
+    from exact_io_aware_40_gb300 import fa
+    fake, null, f = ctypes.c_void_p(0x10000), ctypes.c_void_p(0), ctypes.c_float
+    assert fa.fa_fwd_fp8_workspace_bytes(1, 2, 100, 128) == (2 * 128 * 112 + 255) // 256 * 256
+    assert fa.fa_fwd_fp8_workspace_bytes(1, 2, 100, 64) == 0
+    call = lambda d, dq, ws_bytes: lib.fa_fwd_fp8(*([fake] * 5), 1, 2, 100, d, f(0.1), f(dq), f(1.0),
+                                                  f(1.0), 1, null, fake, ws_bytes, null)
+    assert call(64, 1.0, 1 << 20) == 2          # d must be 128
+    assert call(128, 0.0, 1 << 20) == 1         # descale factor must be > 0
+    assert call(128, float("inf"), 1 << 20) == 1
+    assert call(128, 1.0, 64) == 1              # short workspace

@@ -42,3 +42,33 @@ def test_kv_lengths_range():
     assert kl.dtype == np.int32
     assert kl.min() >= 256 and kl.max() <= 512
     assert kl.min() < 270 and kl.max() > 500
+
+
+# --- e4m3 codes of the 8-bit forward ------------------------------------------
+
+def test_e4m3_decoding_follows_the_format():
+    # sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 subnormal;
+    # 0x7F / 0xFF NaN, no infinities
+    v = inputs.e4m3_bits_to_f64(np.arange(256, dtype=np.uint8))
+    assert v[0x00] == 0.0 and v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9
+    assert v[0x08] == 2.0 ** -6 and v[0x38] == 1.0 and v[0x39] == 1.125 and v[0x40] == 2.0
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0 and v[0xB8] == -1.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isnan(v).sum() == 2
+    fin = v[~np.isnan(v)]
+    assert np.all(np.diff(v[:0x7F]) > 0)  # codes 0..0x7E strictly increasing
+    assert fin.max() == 448.0
+
+
+def test_e4m3_encoding_rounds_to_nearest_even_and_saturates():
+    codes = np.arange(256, dtype=np.uint8)
+    v = inputs.e4m3_bits_to_f64(codes)
+    fin = ~np.isnan(v)
+    np.testing.assert_array_equal(inputs.f32_to_e4m3_bits(v[fin]), codes[fin])
+    # ties go to the even code; beyond 448 saturates
+    assert list(inputs.f32_to_e4m3_bits([1.0625, 1.1875, 3 * 2.0 ** -10, 500.0, -1e9])) == [
+        0x38, 0x3A, 0x02, 0x7E, 0xFE]
+    # nearest: a random sample against brute force over the finite codes
+    x = np.random.default_rng(5).normal(0, 3, 2000)
+    got = inputs.e4m3_bits_to_f64(inputs.f32_to_e4m3_bits(x))
+    best = np.abs(x[:, None] - v[fin][None, :]).min(axis=1)
+    np.testing.assert_allclose(np.abs(got - x), best, rtol=0, atol=0)
