@@ -568,6 +568,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
 cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream) {
+  if (fwd_one_block(d, a.N, a.window, a.bmask, a.drop_thr))
+    return launch_fwd_1q(d, tmQ, tmK, tmV, tmO, a, stream);
   switch (d) {
     case 64:
       return a.drop_thr ? launch_fwd_t<64, true>(tmQ, tmK, tmV, tmO, a, stream)
@@ -575,7 +577,6 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
     case 128:
       return a.drop_thr ? launch_fwd_t<128, true>(tmQ, tmK, tmV, tmO, a, stream)
                         : launch_fwd_t<128, false>(tmQ, tmK, tmV, tmO, a, stream);
-    case 256: return launch_fwd_d256(tmQ, tmK, tmV, tmO, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

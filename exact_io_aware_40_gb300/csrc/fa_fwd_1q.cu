@@ -1,14 +1,19 @@
-// fa_fwd_d256.cu -- forward pass of exact attention for head dimension 256.
+// fa_fwd_1q.cu -- forward pass of exact attention with one query block per
+// CTA: head dimension 256, and short sequences at d = 64 and 128.
 //
 // Same method as fa_fwd.cu (tiling, masked online softmax with running row
 // max and sum, O accumulated on chip; study notes "FlashAttention学习笔记",
 // section "分块计算整体流程(Tiling)"; apxml.com chapter "高效注意力算法实现
 // (FlashAttention)", section "在线Softmax").  With d = 256 the O accumulator of
 // one 128-row query block alone fills 256 TMEM columns and a 128 x 256 bf16
-// tile is 64 KB, so the layout differs from the d <= 128 kernel:
+// tile is 64 KB, so the two-block layout of fa_fwd.cu does not fit.  For short
+// sequences at d <= 128 the same small layout (256 TMEM columns, under 100 KB
+// of shared memory) lets two CTAs share an SM, so one CTA's set-up, pipeline
+// fill and epilogue overlap the other's work -- with only a few key blocks
+// per CTA those fixed costs dominate.
 //   - one 128-row query block per CTA; key blocks of 64 rows;
 //   - TMEM: two S buffers of 64 columns (S_j = Q K_j^T double-buffered so the
-//     product for block j+1 overlaps the softmax of block j) and O (256
+//     product for block j+1 overlaps the softmax of block j) and O (d
 //     columns);
 //   - warp 0: TMA producer (Q once; K_j, V_j through 2-stage rings);
 //     warp 1: tcgen05 issuer; warps 2-5: softmax (thread = query row = TMEM
@@ -45,11 +50,15 @@ struct Cfg {
   static constexpr int kNumBar = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kUsed = kOffMisc + 16;
-  static constexpr int kSmemBytes = kUsed + 1024;  // + alignment of the base
+  // d <= 128: at least 100 KB, so no more than two CTAs (two 256-column TMEM
+  // allocations) are resident on an SM.
+  static constexpr int kSmemBytes =
+      HD == 256 ? kUsed + 1024 : (kUsed + 1024 > 102400 ? kUsed + 1024 : 102400);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // TMEM columns
+  // TMEM columns: S buffers at 0 and 64, O at 128
   static constexpr uint32_t kColO = 128;
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemCols = HD == 256 ? 512 : 256;
+  static constexpr int kMinBlocks = HD == 256 ? 1 : 2;
 };
 
 __device__ __forceinline__ uint32_t s_col(int b) { return b ? 64u : 0u; }
@@ -69,8 +78,8 @@ __device__ __forceinline__ bool bar_and_128(int id, bool pred) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
+    fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdArgs a) {
   using C = Cfg<HD>;
@@ -411,7 +420,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_fwd_d256_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_fwd_1q_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -419,17 +428,22 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_d256_kernel<HD><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
+  fa_fwd_1q_kernel<HD><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
                                                                                     tmO, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_d256(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                            const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
-                            cudaStream_t stream) {
-  return launch_fwd_t<256>(tmQ, tmK, tmV, tmO, a, stream);
+cudaError_t launch_fwd_1q(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
+                          cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch_fwd_t<64>(tmQ, tmK, tmV, tmO, a, stream);
+    case 128: return launch_fwd_t<128>(tmQ, tmK, tmV, tmO, a, stream);
+    case 256: return launch_fwd_t<256>(tmQ, tmK, tmV, tmO, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fa

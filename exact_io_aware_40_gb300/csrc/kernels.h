@@ -29,12 +29,22 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream);
 
-// Forward for d = 256 (one 128-row query block per CTA, 64-key blocks; the
-// K and V maps use 64-row boxes).  grid = ceil(N/128) * BH.
-cudaError_t launch_fwd_d256(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                            const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
-                            cudaStream_t stream);
-inline int fwd_kv_rows(int d) { return d == 256 ? 64 : 128; }
+// Forward with one 128-row query block per CTA and 64-key blocks (the K and
+// V maps use 64-row boxes), two CTAs per SM at d = 64 and 128, one at d = 256.
+// Causal and key padding only.  grid = ceil(N/128) * BH.
+cudaError_t launch_fwd_1q(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
+                          cudaStream_t stream);
+// The forward kernel for a call: the one-block kernel unless a window, block
+// mask or dropout needs the two-block kernel of fa_fwd.cu.  (Measured on the
+// sweep, the one-block kernel with two CTAs per SM is 1.4-1.9x faster at
+// N <= 1024 and level at N = 16384, d = 128.)
+inline bool fwd_one_block(int d, int N, int window, const void* bmask, uint32_t drop_thr) {
+  (void)N;
+  return d == 256 || (window < 0 && bmask == nullptr && drop_thr == 0);
+}
+// Rows of the K and V boxes of the kernel fwd_one_block picks.
+inline int fwd_kv_rows(bool one_block) { return one_block ? 64 : 128; }
 
 // e4m3 forward, d = 128 (fa_fwd_fp8.cu): V [BH, N, 128] -> V^T [BH, 128,
 // Npad] (Npad = N rounded up to 16, zero-filled), then the forward with Q, K

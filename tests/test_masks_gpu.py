@@ -101,9 +101,13 @@ def test_block_sparse_empty_rows_window_and_padding(d):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_masks_that_change_nothing_are_bitwise_identical(d, causal):
-    # an all-ones block mask and a window wider than the sequence (with the
-    # causal term it implies) visit the same tiles with the same element masks
+def test_masks_that_change_nothing_change_nothing(d, causal):
+    # An all-ones block mask, and a window wider than the sequence (with the
+    # causal term it implies), keep every pair.  The forward then runs on the
+    # two-block kernel instead of the one-block one (a different summation
+    # order: agreement to a few bf16 ulps); the backward kernels visit the
+    # same tiles with the same element masks: given the same O and L they
+    # agree bit for bit.
     from exact_io_aware_40_gb300 import fa
     N = 777
     case = H.Case(1501, 1, 3, N, d)
@@ -111,17 +115,17 @@ def test_masks_that_change_nothing_are_bitwise_identical(d, causal):
     o0, L0 = fa.attention_fwd(q, k, v, causal=causal, scale=case.scale)
     g0 = fa.attention_bwd(q, k, v, o0, do, L0, causal=causal, scale=case.scale)
     ones = dev_mask(np.ones(((N + 127) // 128,) * 2, np.uint8))
-    o1, L1 = fa.attention_fwd(q, k, v, causal=causal, scale=case.scale, block_mask=ones)
-    g1 = fa.attention_bwd(q, k, v, o1, do, L1, causal=causal, scale=case.scale, block_mask=ones)
-    fa.fa_check_error()
-    assert bool((o0 == o1).all()) and bool((L0 == L1).all())
-    assert all(bool((a == b).all()) for a, b in zip(g0, g1))
+    variants = [dict(block_mask=ones, causal=causal)]
     if causal:
-        o2, L2 = fa.attention_fwd(q, k, v, causal=False, scale=case.scale, window=N)
-        g2 = fa.attention_bwd(q, k, v, o2, do, L2, causal=False, scale=case.scale, window=N)
+        variants.append(dict(window=N, causal=False))
+    for kw in variants:
+        o1, L1 = fa.attention_fwd(q, k, v, scale=case.scale, **kw)
+        g1 = fa.attention_bwd(q, k, v, o0, do, L0, scale=case.scale, **kw)
         fa.fa_check_error()
-        assert bool((o0 == o2).all()) and bool((L0 == L2).all())
-        assert all(bool((a == b).all()) for a, b in zip(g0, g2))
+        a0, a1 = H.to_f64(o0), H.to_f64(o1)
+        assert float(np.abs(a0 - a1).max()) <= 2.0 ** -6 * max(1.0, float(np.abs(a0).max()))
+        assert float(np.abs(H.to_f64(L0) - H.to_f64(L1)).max()) <= 1e-5
+        assert all(bool((x == y).all()) for x, y in zip(g0, g1))
 
 
 @pytest.mark.parametrize("kind", ["window", "block_sparse"])
