@@ -75,6 +75,24 @@ def step_flops(b=None, h=None, n=None, d=D):
     return sum(14 * d * pairs(c, b, h, n) for c in (0, 1))
 
 
+def max_over_ranks(value, world, device):
+    """The largest value over all ranks (the slowest rank's time); the value
+    itself for a single rank.  All ranks must call it together."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step, world, ms_per_step):
+    """Whole-job TFLOP/s: every rank runs the same step (independent replicas),
+    so the job does world x the FLOPs of one rank in the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -343,13 +361,10 @@ def run_masked(args, rank, world):
     ms_step = t0.elapsed_time(t1) / args.steps
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, world, dev)
     P = B * H * per_head
     flops = 14 * D * P
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms_step)
 
     host_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
                 for n, t in (("o", o), ("L", L), ("dq", dq), ("dk", dk), ("dv", dv))}
@@ -479,12 +494,9 @@ def run_fp8(args, rank, world):
     fa.fa_check_error(sp)
     ms_step = t0.elapsed_time(t1) / args.steps
     per_c = {c: sum(e[c][0].elapsed_time(e[c][1]) for e in evs) / args.steps for c in (0, 1)}
-    if world > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, world, dev)
     flops = sum(4 * D * pairs(c) for c in (0, 1))
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms_step)
     host_out = {c: (torch.empty(out[c][0].shape, dtype=torch.bfloat16).pin_memory(),
                     torch.empty(out[c][1].shape, dtype=torch.float32).pin_memory()) for c in (0, 1)}
     h2d = sum(host[n].numel() for n in ("Q", "K", "V"))
@@ -704,12 +716,9 @@ def run_ours(args, rank, world):
             for i, st in enumerate(stages):
                 per_stage[c][st] += evs[s][c][i].elapsed_time(evs[s][c][i + 1])
     ms_step = ms_total / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, world, dev)
     flops = step_flops()
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms_step)
 
     # ---- end to end: pinned host inputs -> device, both passes, results -> pinned host
     host_out = {c: {n: torch.empty(out[c][n].shape, dtype=out[c][n].dtype).pin_memory()
@@ -739,10 +748,7 @@ def run_ours(args, rank, world):
     barrier()
     fa.fa_check_error(sp)
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(ms_e2e, world, dev)
 
     if rank != 0:
         return

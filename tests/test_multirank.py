@@ -1,0 +1,73 @@
+"""The multi-rank path of bench.py, on CPU: a gloo process group of two ranks.
+
+Every (batch, head) is independent, so N GPUs run N independent replicas of
+the step with no collective on the data path; the only cross-rank operations
+are the barriers around the timed region and the max over ranks of the step
+time, and rank 0 alone prints.  These tests run those pieces with gloo."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    slowest = bench.max_over_ranks(1.5 + rank, world, "cpu")   # rank r took 1.5 + r ms
+    dist.barrier()
+    dist.destroy_process_group()
+    out.put((rank, slowest))
+
+
+def test_max_over_ranks_with_gloo_world_size_2():
+    torch = pytest.importorskip("torch")
+    ctx = torch.multiprocessing.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 2.5), (1, 2.5)]
+
+
+def test_job_throughput_counts_every_replica():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.job_throughput(2e12, 1, 1000.0) == pytest.approx(2.0)
+    assert bench.job_throughput(2e12, 4, 1000.0) == pytest.approx(8.0)
+    assert bench.max_over_ranks(3.0, 1, "cpu") == 3.0
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    pytest.importorskip("torch")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
