@@ -10,8 +10,9 @@
 // the loads of Q, K, V and the store of O and L stays on chip (study notes,
 // section "Kernel融合").
 //
-// GB300 mapping: one CTA owns two 128-row query blocks A and B of one
-// (batch, head) and streams K_j, V_j once for both.
+// This kernel serves the calls with a sliding window, a block mask or dropout
+// (fa_fwd_1q.cu serves the rest).  GB300 mapping: one CTA owns two 128-row
+// query blocks A and B of one (batch, head) and streams K_j, V_j once for both.
 //   warp 0      TMA producer: Q_A, Q_B once; K_j, V_j through smem rings
 //               (128-byte swizzle, 64-column atoms).
 //   warp 1      tcgen05 issuer (one thread), per key block j:
@@ -568,7 +569,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
 cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream) {
-  if (fwd_one_block(d, a.N, a.window, a.bmask, a.drop_thr))
+  if (fwd_one_block(d, a.window, a.bmask, a.drop_thr))
     return launch_fwd_1q(d, tmQ, tmK, tmV, tmO, a, stream);
   switch (d) {
     case 64:

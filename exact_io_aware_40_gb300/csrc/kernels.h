@@ -24,7 +24,7 @@ struct FwdArgs {
   float out_scale;      // factor applied to O (e4m3 forward: V's dequantisation factor)
 };
 
-// Forward: grid = n_qtiles * BH CTAs.
+// Forward (dispatches between the two forward kernels, see fwd_one_block).
 cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream);
@@ -39,8 +39,7 @@ cudaError_t launch_fwd_1q(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
 // mask or dropout needs the two-block kernel of fa_fwd.cu.  (Measured on the
 // sweep, the one-block kernel with two CTAs per SM is 1.4-1.9x faster at
 // N <= 1024 and level at N = 16384, d = 128.)
-inline bool fwd_one_block(int d, int N, int window, const void* bmask, uint32_t drop_thr) {
-  (void)N;
+inline bool fwd_one_block(int d, int window, const void* bmask, uint32_t drop_thr) {
   return d == 256 || (window < 0 && bmask == nullptr && drop_thr == 0);
 }
 // Rows of the K and V boxes of the kernel fwd_one_block picks.
