@@ -211,9 +211,8 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
   if ((st = map_bf16(enc, &tq, Q, d, N, BH, 128)) != FA_OK) return st;
-  const int kv_rows = fa::fwd_kv_rows(fa::fwd_one_block(d, window, block_mask, drop.thr));
-  if ((st = map_bf16(enc, &tk, K, d, N, BH, kv_rows)) != FA_OK) return st;
-  if ((st = map_bf16(enc, &tv, V, d, N, BH, kv_rows)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tk, K, d, N, BH, fa::kFwdKvRows)) != FA_OK) return st;
+  if ((st = map_bf16(enc, &tv, V, d, N, BH, fa::kFwdKvRows)) != FA_OK) return st;
   if ((st = map_bf16(enc, &to, O, d, N, BH, 128)) != FA_OK) return st;
   fa::FwdArgs a;
   a.L = L;

@@ -10,24 +10,24 @@
 // the loads of Q, K, V and the store of O and L stays on chip (study notes,
 // section "Kernel融合").
 //
-// This kernel serves the calls with a sliding window, a block mask or dropout
-// (fa_fwd_1q.cu serves the rest).  GB300 mapping: one CTA owns two 128-row
-// query blocks A and B of one (batch, head) and streams K_j, V_j once for both.
-//   warp 0      TMA producer: Q_A, Q_B once; K_j, V_j through smem rings
-//               (128-byte swizzle, 64-column atoms).
-//   warp 1      tcgen05 issuer (one thread), per key block j:
-//                 O_A += P_A V_j;  S_A = Q_A K_{j+1}^T;  O_B += P_B V_j;  S_B = Q_B K_{j+1}^T
-//               so while one softmax warpgroup works on its S the tensor pipe
-//               runs the other block's products.  Owns TMEM (512 columns:
-//               S_A, S_B at 0 and 128, O_A, O_B at 256 and 256 + d).
-//   warps 4-7   softmax of block A, warps 8-11 softmax of block B: thread t
-//               owns query row t (= TMEM lane t); reads its S row, masks,
-//               updates (m, l), writes P (bf16) over the first 64 columns of
-//               its S buffer, rescales its O row in TMEM when the row maximum
-//               grew by more than 2^8, and finally writes O / l (TMA store) and L.
-// The commit that announces S_X(j+1) also covers every earlier product of the
-// issuing thread, PV_X(j) included, so O_X is stable whenever its softmax
-// warpgroup holds a fresh S_X: the rescale needs no extra wait.
+// GB300 mapping: one 128-row query block per CTA, key blocks of 64 rows.
+//   - TMEM: two S buffers of 64 columns (S_j = Q K_j^T double-buffered so the
+//     product for block j+1 overlaps the softmax of block j) and O (d
+//     columns) -- 256 columns for d <= 128, so with under 100 KB of shared
+//     memory two CTAs share an SM and one CTA's set-up, pipeline fill and
+//     epilogue overlap the other's products (d = 256: 512 columns, one CTA);
+//   - warp 0: TMA producer (Q once; K_j, V_j through 2-stage rings, 128-byte
+//     swizzle, 64-column atoms); warp 1: tcgen05 issuer (one thread) and TMEM
+//     owner; warps 2-5: softmax (thread = query row = TMEM lane): reads its S
+//     row, masks, updates (m, l), writes P (bf16) back to TMEM for the PV
+//     product, rescales its O row only when the row maximum grew by more than
+//     2^8, and finally writes O / l (TMA store) and L.
+// The commit that announces S(j+1) also covers every earlier product of the
+// issuing thread, PV(j) included, so O is stable whenever the softmax holds a
+// fresh S: the rescale needs no extra wait.
+// Key blocks are visited in the order of the tile walk of masks.cuh: the
+// contiguous range that kv_len, causal and window leave, thinned by the block
+// mask; elements are masked only in blocks that cross a boundary.
 // Loop order: query block outer (per CTA), key block inner, so O stays in TMEM
 // for the whole loop; the study notes' K/V-outer order computes the same
 // result (they only differ in which operand is reused on chip).
@@ -41,62 +41,63 @@
 namespace fa {
 namespace {
 
-constexpr int kBR = 128;      // query rows per block (MMA M)
-constexpr int kBC = 128;      // keys per block (MMA N of S, K of PV)
-constexpr int kThreads = 384;
-// Registers per thread after setmaxnreg: warps 0-3 (producer, MMA) and the
-// softmax warpgroups.  The dropout variant moves 8 more to the softmax, which
-// also runs the random-number generator.
-template <bool DROP> constexpr int kRegsLow = DROP ? 56 : 64;
-template <bool DROP> constexpr int kRegsHigh = DROP ? 224 : 216;
+constexpr int kBR = 128;      // query rows per CTA (MMA M)
+constexpr int kBC = 64;       // keys per block (MMA N of S, K of PV)
+constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 8
 constexpr float kLn2 = 0.693147180559945309f;
 
 template <int HD>
 struct Cfg {
   static constexpr int kAtoms = HD / 64;                 // 64-column swizzle atoms
-  static constexpr int kAtomBytes = kBR * 128;           // 128 rows x 128 B
+  static constexpr int kAtomBytes = kBR * 128;           // 128 rows x 128 B (Q, O)
   static constexpr int kTileBytes = kAtoms * kAtomBytes; // one 128-row bf16 tile
-  static constexpr int kKSt = HD == 64 ? 3 : 2;
-  static constexpr int kVSt = HD == 64 ? 3 : 2;
-  static constexpr int kOffQ = 0;                          // Q_A, Q_B
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kKSt * kTileBytes;
-  static constexpr int kOffBar = kOffV + kVSt * kTileBytes;
-  // q_full[2], k_full[], k_empty[], v_full[], v_empty[], s_full[2], p_full[2],
-  // o_final[2], drain
-  static constexpr int kNumBar = 2 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1;
-  // misc: tmem slot, abort flag, then the key-block walk (TA, TB, lo[2], hi[2], ulo, uhi)
+  static constexpr int kKVAtom = kBC * 128;              // 64 rows x 128 B (K, V)
+  static constexpr int kKVTile = kAtoms * kKVAtom;
+  static constexpr int kKSt = 2;
+  static constexpr int kVSt = 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kKSt * kKVTile;
+  static constexpr int kOffBar = kOffV + kVSt * kKVTile;
+  // barriers: q_full, k_full[], k_empty[], v_full[], v_empty[], s_full[2],
+  // p_full[2], o_done, drain
+  static constexpr int kNumBar = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
-  static constexpr int kUsed = kOffMisc + 48;
-  static constexpr int kSmemBytes = kUsed + 1024;  // + alignment of the base
+  static constexpr int kUsed = kOffMisc + 16;
+  // d <= 128: at least 100 KB, so no more than two CTAs (two 256-column TMEM
+  // allocations) are resident on an SM.
+  static constexpr int kSmemBytes =
+      HD == 256 ? kUsed + 1024 : (kUsed + 1024 > 102400 ? kUsed + 1024 : 102400);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static constexpr uint32_t kColO = 256;
-  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: S buffers at 0 and 64, O at 128
+  static constexpr uint32_t kColO = 128;
+  static constexpr uint32_t kTmemCols = HD == 256 ? 512 : 256;
+  static constexpr int kMinBlocks = HD == 256 ? 1 : 2;
 };
 
-// Named barrier over `n` threads that also returns the AND of `pred` over them.
-__device__ __forceinline__ bool bar_and(int id, int n, bool pred) {
+__device__ __forceinline__ uint32_t s_col(int b) { return b ? 64u : 0u; }
+
+// Named barrier over 128 threads that also returns the AND of `pred` over them.
+__device__ __forceinline__ bool bar_and_128(int id, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "r"(pred ? 1u : 0u), "r"(id)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
-// DROP: dropout on P (a separate instantiation, so the kernel without it
-// carries none of its code).
-template <int HD, bool DROP>
-__global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+// DROP: dropout on P; MASKX: a sliding window or a block mask.  Separate
+// instantiations, so the kernel without them carries none of their code
+// (the window and block-mask terms cost the plain case a few per cent).
+template <int HD, bool DROP, bool MASKX>
+__global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
+    fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdArgs a) {
   using C = Cfg<HD>;
@@ -110,16 +111,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = sb + C::kOffK;
   const uint32_t sV = sb + C::kOffV;
   const uint32_t bar0 = sb + C::kOffBar;
-  auto bar_qfull = [&](int x) { return bar0 + 8u * x; };
-  auto bar_kfull = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto bar_kempty = [&](int s) { return bar0 + 8u * (2 + C::kKSt + s); };
-  auto bar_vfull = [&](int s) { return bar0 + 8u * (2 + 2 * C::kKSt + s); };
-  auto bar_vempty = [&](int s) { return bar0 + 8u * (2 + 2 * C::kKSt + C::kVSt + s); };
-  const uint32_t bar_s0 = bar0 + 8u * (2 + 2 * C::kKSt + 2 * C::kVSt);
-  auto bar_sfull = [&](int x) { return bar_s0 + 8u * x; };
-  auto bar_pfull = [&](int x) { return bar_s0 + 16u + 8u * x; };
-  auto bar_ofinal = [&](int x) { return bar_s0 + 32u + 8u * x; };
-  const uint32_t bar_drain = bar_s0 + 48u;
+  const uint32_t bar_q = bar0;
+  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_kempty = [&](int s) { return bar0 + 8u * (1 + C::kKSt + s); };
+  auto bar_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * C::kKSt + s); };
+  auto bar_vempty = [&](int s) { return bar0 + 8u * (1 + 2 * C::kKSt + C::kVSt + s); };
+  const uint32_t bar_sfull0 = bar0 + 8u * (1 + 2 * C::kKSt + 2 * C::kVSt);
+  const uint32_t bar_pfull0 = bar_sfull0 + 16u;
+  const uint32_t bar_odone = bar_pfull0 + 16u;
+  const uint32_t bar_drain = bar_odone + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -127,59 +127,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // Head-major order with the longest query blocks (causal) of a head first.
-  const int n_pairs = (a.n_qtiles + 1) / 2;
-  const int bh = static_cast<int>(blockIdx.x / n_pairs);
-  const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs);
-  const int qtA = 2 * pr;
+  // Head-major order: the CTAs in flight share one head's K/V (L2 reuse); within
+  // a head the longest query blocks (causal) start first.
+  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
+  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
+  const int q0 = qt * kBR;
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const bool hasB = qtA + 1 < a.n_qtiles;
-  // Key blocks each query block can see: a range from the key padding, causal
-  // and window terms, thinned by the block mask.  The CTA walks the union of
-  // both blocks' lists in increasing order (each K_j, V_j is loaded once);
-  // block X processes the first T_X entries of the walk, and an entry inside
-  // that prefix that X does not see is computed fully masked.
-  // The walk (T_A, T_B, lo[2], hi[2], ulo, uhi) is set up once by warp 3.
-  int* walk = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
-  if (warp == 3) {
-    int loA, hiA, loB = 0, hiB = 0;
-    key_block_range(qtA, kv_limit, a.causal, a.window, &loA, &hiA);
-    if (hasB) key_block_range(qtA + 1, kv_limit, a.causal, a.window, &loB, &hiB);
-    const int ulo = loB < hiB ? min(loA, loB) : loA;
-    const int uhi = max(hiA, hiB);
-    const uint8_t* bmA = a.bmask ? a.bmask + static_cast<long long>(qtA) * a.nb : nullptr;
-    const uint8_t* bmB = (a.bmask && hasB) ? a.bmask + static_cast<long long>(qtA + 1) * a.nb : nullptr;
-    // T_A, T_B: entry index (+1) of the last block each query block sees.
-    int n = 0, ta = 0, tb = 0;
-    for (int b0 = ulo; b0 < uhi; b0 += 32) {
+  // The 64-key blocks this query block visits: a range from the key padding,
+  // causal and window terms, thinned by row qt of the block mask (whose
+  // 128-key blocks are pairs of 64-key blocks).  Every role walks the same
+  // list; warp 2 counts it.
+  const int window = MASKX ? a.window : -1;
+  int klo, khi;
+  {
+    int h = (kv_limit + kBC - 1) / kBC;
+    if (a.causal || window >= 0) h = min(h, 2 * qt + 2);  // keys <= q0 + 127
+    const int l = window >= 0 ? max(0, q0 - window) / kBC : 0;
+    klo = l;
+    khi = max(h, l);
+  }
+  const uint8_t* bmr =
+      (MASKX && a.bmask) ? a.bmask + static_cast<long long>(qt) * a.nb : nullptr;
+  auto next_kb = [&](int kb) -> int {  // next visited 64-key block at or after kb
+    if constexpr (MASKX) {
+      if (bmr == nullptr) return kb;
+      while (kb < khi && !block_on(bmr, 1, kb >> 1)) ++kb;
+    }
+    return kb;
+  };
+  volatile int* n_steps = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+  if (MASKX && warp == 2 && bmr != nullptr) {
+    int n = 0;
+    for (int b0 = klo; b0 < khi; b0 += 32) {
       const int kb = b0 + lane;
-      const bool sa = kb < uhi && kb >= loA && kb < hiA && block_on(bmA, 1, kb);
-      const bool sb2 = kb < uhi && kb >= loB && kb < hiB && block_on(bmB, 1, kb);
-      const uint32_t on = __ballot_sync(0xffffffffu, sa || sb2);
-      const int idx = n + __popc(on & ((1u << lane) - 1u));
-      ta = max(ta, sa ? idx + 1 : 0);
-      tb = max(tb, sb2 ? idx + 1 : 0);
-      n += __popc(on);
+      n += __popc(__ballot_sync(0xffffffffu, kb < khi && block_on(bmr, 1, kb >> 1)));
     }
-    ta = __reduce_max_sync(0xffffffffu, ta);
-    tb = __reduce_max_sync(0xffffffffu, tb);
-    if (lane == 0) {
-      walk[0] = ta;
-      walk[1] = tb;
-      walk[2] = loA;
-      walk[3] = loB;
-      walk[4] = hiA;
-      walk[5] = hiB;
-      walk[6] = ulo;
-      walk[7] = uhi;
-    }
+    if (lane == 0) *n_steps = n;
   }
 
   if (tid == 0) {
-    mbar_init(bar_qfull(0), 1);
-    mbar_init(bar_qfull(1), 1);
+    mbar_init(bar_q, 1);
     for (int s = 0; s < C::kKSt; ++s) {
       mbar_init(bar_kfull(s), 1);
       mbar_init(bar_kempty(s), 1);
@@ -188,11 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_vfull(s), 1);
       mbar_init(bar_vempty(s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar_sfull(x), 1);
-      mbar_init(bar_pfull(x), 4);
-      mbar_init(bar_ofinal(x), 1);
-    }
+    mbar_init(bar_sfull0, 1);
+    mbar_init(bar_sfull0 + 8, 1);
+    mbar_init(bar_pfull0, 4);
+    mbar_init(bar_pfull0 + 8, 4);
+    mbar_init(bar_odone, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -210,50 +199,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
-  const int TA = walk[0], TB = walk[1];
-  const int T = max(TA, TB);
-  // Bounds re-read from shared memory at each use: kept in registers they
-  // push the producer and softmax warps past their register budgets.
-  volatile int* vw = walk;
-  const int ulo = walk[6];
-  auto sees = [&](int x, int kb) -> bool {  // does query block X see key block kb?
-    const uint8_t* row = a.bmask ? a.bmask + static_cast<long long>(qtA + x) * a.nb : nullptr;
-    return kb >= vw[2 + x] && kb < vw[4 + x] && block_on(row, 1, kb);
-  };
-  auto next_kb = [&](int kb) -> int {  // next entry of the walk at or after kb
-    const int uhi = vw[7];
-    while (kb < uhi && !sees(0, kb) && !sees(1, kb)) ++kb;
-    return kb;
-  };
+  // Without a block mask the list is the whole range (no count to read).
+  const int T = bmr ? *n_steps : khi - klo;
 
-  if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow<DROP>));
-    if (warp == 0 && lane == 0 && T > 0) {
-      // ---------------------------------------------------------- producer
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && T > 0) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      for (int x = 0; x < (hasB ? 2 : 1); ++x) {
-        mbar_arrive_expect_tx(bar_qfull(x), C::kTileBytes);
-        for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(sQ + x * C::kTileBytes + c * C::kAtomBytes, &tmQ, c * 64, (qtA + x) * kBR, bh,
-                      bar_qfull(x), pol_q);
-      }
+      mbar_arrive_expect_tx(bar_q, C::kTileBytes);
+      for (int c = 0; c < C::kAtoms; ++c)
+        tma_load_3d(sQ + c * C::kAtomBytes, &tmQ, c * 64, q0, bh, bar_q, pol_q);
       int last_k[C::kKSt], last_v[C::kVSt];
       for (int s = 0; s < C::kKSt; ++s) last_k[s] = -1;
       for (int s = 0; s < C::kVSt; ++s) last_v[s] = -1;
-      int kb = next_kb(ulo);
+      int kb = next_kb(klo);
       for (int j = 0; j < T; ++j, kb = next_kb(kb + 1)) {
         const int ks = j % C::kKSt, vs = j % C::kVSt;
         if (j >= C::kKSt && !mbar_wait(bar_kempty(ks), ((j / C::kKSt) & 1) ^ 1, ab)) break;
-        mbar_arrive_expect_tx(bar_kfull(ks), C::kTileBytes);
+        mbar_arrive_expect_tx(bar_kfull(ks), C::kKVTile);
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(sK + ks * C::kTileBytes + c * C::kAtomBytes, &tmK, c * 64, kb * kBC, bh,
+          tma_load_3d(sK + ks * C::kKVTile + c * C::kKVAtom, &tmK, c * 64, kb * kBC, bh,
                       bar_kfull(ks), pol_kv);
         last_k[ks] = j;
         if (j >= C::kVSt && !mbar_wait(bar_vempty(vs), ((j / C::kVSt) & 1) ^ 1, ab)) break;
-        mbar_arrive_expect_tx(bar_vfull(vs), C::kTileBytes);
+        mbar_arrive_expect_tx(bar_vfull(vs), C::kKVTile);
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(sV + vs * C::kTileBytes + c * C::kAtomBytes, &tmV, c * 64, kb * kBC, bh,
+          tma_load_3d(sV + vs * C::kKVTile + c * C::kKVAtom, &tmV, c * 64, kb * kBC, bh,
                       bar_vfull(vs), pol_kv);
         last_v[vs] = j;
       }
@@ -261,134 +233,127 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Unwinding: let the copies already issued land before the CTA exits.
         // Load j is the (j / stages)-th use of its stage, so its completion is
         // the phase of that parity.
-        mbar_wait_drain(bar_qfull(0), 0);
-        if (hasB) mbar_wait_drain(bar_qfull(1), 0);
+        mbar_wait_drain(bar_q, 0);
         for (int s = 0; s < C::kKSt; ++s)
           if (last_k[s] >= 0) mbar_wait_drain(bar_kfull(s), (last_k[s] / C::kKSt) & 1);
         for (int s = 0; s < C::kVSt; ++s)
           if (last_v[s] >= 0) mbar_wait_drain(bar_vfull(s), (last_v[s] / C::kVSt) & 1);
       }
-    } else if (warp == 1 && lane == 0 && T > 0) {
-      // ---------------------------------------------------------- MMA issuer
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
       constexpr uint32_t idS = idesc_bf16(kBR, kBC, false, false);
       constexpr uint32_t idO = idesc_bf16(kBR, HD, false, true);
-      bool ok = true;
-      // S_X(j) = Q_X K_j^T into S buffer X (columns 128 X).
-      auto issue_s = [&](int x, int j) -> bool {
-        const int ks = j % C::kKSt;
-        if (j == 0 && !mbar_wait(bar_qfull(x), 0, ab)) return false;
-        if (!mbar_wait(bar_kfull(ks), (j / C::kKSt) & 1, ab)) return false;
+      bool ok = mbar_wait(bar_q, 0, ab);
+      auto issue_pv = [&](int jj) -> bool {
+        const int bb = jj & 1, vs = jj % C::kVSt;
+        if (!mbar_wait(bar_pfull0 + 8u * bb, (jj >> 1) & 1, ab)) return false;
+        if (!mbar_wait(bar_vfull(vs), (jj / C::kVSt) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t qbase = sQ + x * C::kTileBytes, kbase = sK + ks * C::kTileBytes;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          // K-major operands: step k covers columns [16k, 16k+16) of d, i.e.
-          // atom k/4, byte offset 32*(k%4) inside the 128-byte swizzled row.
-          const uint32_t off = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
-          mma_ss(tmem + 128u * x, sdesc_sw128(qbase + off, 16, 1024),
-                 sdesc_sw128(kbase + off, 16, 1024), idS, k > 0 ? 1u : 0u);
-        }
-        mma_commit(bar_sfull(x));
-        // the last reader of K_j releases its stage
-        if (x == 1 || j >= TB) mma_commit(bar_kempty(ks));
-        return true;
-      };
-      // O_X (+)= P_X(j) V_j with P_X read from TMEM.
-      auto issue_pv = [&](int x, int j) -> bool {
-        const int vs = j % C::kVSt;
-        if (!mbar_wait(bar_pfull(x), j & 1, ab)) return false;
-        // the first reader of V_j waits for it
-        if ((x == 0 || j >= TA) && !mbar_wait(bar_vfull(vs), (j / C::kVSt) & 1, ab)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sV + vs * C::kTileBytes;
-        const uint32_t ocol = C::kColO + static_cast<uint32_t>(HD) * x;
+        const uint32_t vbase = sV + vs * C::kKVTile;
 #pragma unroll
         for (int k = 0; k < kBC / 16; ++k) {
           // B = V_j, MN-major: 16 key rows per step (two 8-row groups, SBO
           // 1024 B); 64-column atoms of d are kAtomBytes apart (LBO).
-          const uint64_t bdesc = sdesc_sw128(vbase + k * 2048, C::kAtomBytes, 1024);
-          mma_ts(tmem + ocol, tmem + 128u * x + k * 8, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+          const uint64_t bdesc = sdesc_sw128(vbase + k * 2048, C::kKVAtom, 1024);
+          mma_ts(tmem + C::kColO, tmem + s_col(bb) + k * 8, bdesc, idO, (jj > 0 || k > 0) ? 1u : 0u);
         }
-        if (j == (x == 0 ? TA : TB) - 1) mma_commit(bar_ofinal(x));
-        if (x == 1 || j >= TB) mma_commit(bar_vempty(vs));
+        mma_commit(bar_odone);
+        mma_commit(bar_vempty(vs));
         return true;
       };
-      if (TA > 0) ok = issue_s(0, 0);
-      if (ok && TB > 0) ok = issue_s(1, 0);
       for (int j = 0; ok && j < T; ++j) {
-        // S_X(j+1) overwrites P_X(j): the product just before it reads P_X(j)
-        // first (MMAs of one thread execute in issue order).
-        if (j < TA) {
-          ok = issue_pv(0, j);
-          if (ok && j + 1 < TA) ok = issue_s(0, j + 1);
+        const int bb = j & 1, ks = j % C::kKSt;
+        if (j >= 2 && !mbar_wait(bar_odone, (j - 2) & 1, ab)) { ok = false; break; }
+        if (!mbar_wait(bar_kfull(ks), (j / C::kKSt) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kbase = sK + ks * C::kKVTile;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          // K-major operands: step k covers columns [16k, 16k+16) of d, i.e.
+          // atom k/4, byte offset 32*(k%4) inside the 128-byte swizzled row.
+          const uint32_t qoff = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * C::kKVAtom + (k & 3) * 32;
+          mma_ss(tmem + s_col(bb), sdesc_sw128(sQ + qoff, 16, 1024),
+                 sdesc_sw128(kbase + koff, 16, 1024), idS, k > 0 ? 1u : 0u);
         }
-        if (ok && j < TB) {
-          ok = issue_pv(1, j);
-          if (ok && j + 1 < TB) ok = issue_s(1, j + 1);
-        }
+        mma_commit(bar_sfull0 + 8u * bb);
+        mma_commit(bar_kempty(ks));
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
+      if (ok) issue_pv(T - 1);
       // Drain: all MMAs issued above complete before TMEM is released.
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh<DROP>));
     // ------------------------------------------------------------ softmax
-    const int x = (warp >> 2) - 1;          // 0: block A (warps 4-7), 1: block B (warps 8-11)
-    const int Tn = x == 0 ? TA : TB;        // TB = 0 when there is no block B
     const int quarter = warp & 3;           // TMEM lanes [32*quarter, +32)
     const int row = quarter * 32 + lane;    // row of the tile = TMEM lane
-    const int q0 = (qtA + x) * kBR;
     const int grow = q0 + row;              // query index
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t scol = 128u * x;
-    const uint32_t ocol = C::kColO + static_cast<uint32_t>(HD) * x;
     float m_run = -INFINITY;                // running max, log2 units (scaled)
     float l_run = 0.f;                      // row sum of P
     float lh_run = 0.f;                     // row sum of P rounded to bf16
     bool ok = true;
-    int kb = next_kb(ulo);
-    const uint32_t hh = static_cast<uint32_t>(bh % a.H), bb = static_cast<uint32_t>(b);
-    for (int j = 0; j < Tn; ++j) {
-      // Dropout keep bits of this row's 128 keys, drawn while S is computed;
-      // the empty asm keeps the generator from being scheduled among the S
-      // registers below (it would not fit in the register budget there).
-      uint32_t kmask4[4] = {0u, 0u, 0u, 0u};
-      if constexpr (DROP) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          kmask4[c] = keep32(static_cast<uint32_t>(kb * kBC + 32 * c), static_cast<uint32_t>(grow),
-                             hh, bb, a.seed_lo, a.seed_hi, a.drop_thr);
-        asm volatile("" : "+r"(kmask4[0]), "+r"(kmask4[1]), "+r"(kmask4[2]), "+r"(kmask4[3]));
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(x), j & 1, ab))) {
+    const uint32_t hh = static_cast<uint32_t>(bh % a.H), bsq = static_cast<uint32_t>(b);
+    const int q_last = min(q0 + kBR, a.N) - 1;  // last real query row of the block
+    int kb = next_kb(klo);
+    for (int j = 0; j < T; ++j, kb = next_kb(kb + 1)) {
+      const int bb = j & 1;
+      const int key0 = kb * kBC;
+      // Dropout keep bits of this row's 64 keys, drawn before S arrives.
+      uint64_t km = 0;
+      if constexpr (DROP)
+        km = keep32(static_cast<uint32_t>(key0), static_cast<uint32_t>(grow), hh, bsq, a.seed_lo,
+                    a.seed_hi, a.drop_thr) |
+             static_cast<uint64_t>(keep32(static_cast<uint32_t>(key0 + 32),
+                                          static_cast<uint32_t>(grow), hh, bsq, a.seed_lo,
+                                          a.seed_hi, a.drop_thr))
+                 << 32;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull0 + 8u * bb, (j >> 1) & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[4][32];
+      uint32_t sr[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + 32 * c, sr[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(tl + s_col(bb) + 32 * c, sr[c]);
       tmem_wait_ld();
-      const int key0 = kb * kBC;
-      const bool tile_on = sees(x, kb);  // false: a block of the walk X does not see
-      const bool crossing = !tile_on || tile_crosses(q0, key0, a.N, kv_limit, a.causal, a.window);
-      if (crossing) {
+      // Element masking only in blocks holding a key some row does not see
+      // (the window terms kept apart: folded into one expression they change
+      // how the compiler schedules the whole loop, which cost the plain case).
+      bool need_mask = (key0 + kBC > kv_limit) || (a.causal && key0 + kBC - 1 > q0);
+      if constexpr (MASKX)
+        need_mask = need_mask || (window >= 0 && (key0 + kBC - 1 > q0 || key0 < q_last - window));
+      if (need_mask) {
+        if (!MASKX || window < 0) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int key = key0 + 32 * c + e;
-            const bool keep = tile_on & visible(grow, key, kv_limit, a.causal, a.window);
-            sr[c][e] = keep ? sr[c][e] : __float_as_uint(-INFINITY);  // select, no branch
-          }
+            for (int e = 0; e < 32; ++e) {
+              const int key = key0 + 32 * c + e;
+              const bool keep = (key < kv_limit) & !((a.causal != 0) & (key > grow));
+              sr[c][e] = keep ? sr[c][e] : __float_as_uint(-INFINITY);  // select, no branch
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int key = key0 + 32 * c + e;
+              const bool keep = visible(grow, key, kv_limit, a.causal, window);
+              sr[c][e] = keep ? sr[c][e] : __float_as_uint(-INFINITY);
+            }
+        }
       }
       // Row max as a tree (independent partial maxima, no long dependency chain).
       float mxp[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) mxp[t] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(sr[c][e]));
       const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
@@ -402,23 +367,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // add per two elements).  The row sum of P gives L.  O is divided by a
       // second sum, lh: in masked tiles it adds P rounded to bf16 -- the
       // weights the product actually applies to V -- and elsewhere P itself.
-      // A row with fewer than 128 visible keys has no fully visible tile, so
+      // A row with fewer visible keys than a tile has no fully visible tile, so
       // for it lh is exactly the sum of the weights applied, which keeps its O
       // accurate; for longer rows the two sums differ by far less than the
       // bf16 rounding of O.
       const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      float sum_l, sum_h;
       // With dropout the product takes P * Z / q; L and the divisor of O stay
       // the sums of the undropped P.
-      float sum_l, sum_h;
       auto p_tile = [&](auto mode) {
         constexpr bool kRounded = decltype(mode)::value == 1;
         constexpr bool kDrop = decltype(mode)::value == 2;
         uint64_t se[2] = {0ull, 0ull}, sh[2] = {0ull, 0ull};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
-          const uint32_t kmask = kmask4[c];  // dropout keep bits of the chunk's 32 keys
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float t0, t1;
@@ -427,9 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       t0, t1);
             const float p0 = ex2(t0), p1 = ex2(t1);
             if constexpr (kDrop) {
-              const float d0 = (kmask >> (2 * e)) & 1u ? p0 * a.drop_scale : 0.f;
-              const float d1 = (kmask >> (2 * e + 1)) & 1u ? p1 * a.drop_scale : 0.f;
-              pk[e] = pack_bf16(d0, d1);
+              const int kk = 32 * c + 2 * e;
+              pk[e] = pack_bf16((km >> kk) & 1u ? p0 * a.drop_scale : 0.f,
+                                (km >> (kk + 1)) & 1u ? p1 * a.drop_scale : 0.f);
             } else {
               pk[e] = pack_bf16(p0, p1);
             }
@@ -437,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kRounded) sh[e & 1] = f2_add(sh[e & 1], bf16x2_to_f2(pk[e]));
           }
           // P occupies the first 64 columns of the S buffer (2 bf16 per column).
-          tmem_st16(tl + scol + 16 * c, pk);
+          tmem_st16(tl + s_col(bb) + 16 * c, pk);
         }
         float u0, u1;
         f2_unpack(f2_add(se[0], se[1]), u0, u1);
@@ -450,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if constexpr (DROP)
         p_tile(std::integral_constant<int, 2>{});
-      else if (crossing)
+      else if (need_mask)
         p_tile(std::integral_constant<int, 1>{});
       else
         p_tile(std::integral_constant<int, 0>{});
@@ -458,46 +422,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       lh_run = lh_run * alpha + sum_h;
       m_run = m_new;
       if (j > 0 && __any_sync(0xffffffffu, grow_max)) {
-        // O_X holds P_X(0..j-1) V; every product writing it has completed (see
-        // the header), so it can be rescaled in place.
+        // O holds P_0..P_{j-1} V; rescale it once PV_{j-1} has landed.  (Only
+        // PV_{j-1} can be pending: PV_{j-2} completed before S_j was issued, so
+        // the parity of this wait is unambiguous even when earlier ones were
+        // skipped.)
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, ab))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + ocol + 32 * c, o);
-          tmem_wait_ld();
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tl + C::kColO + 32 * c, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tl + ocol + 32 * c, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tl + C::kColO + 32 * c, o);
+          }
         }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull(x));
-      kb = next_kb(kb + 1);
+      if (lane == 0) mbar_arrive(bar_pfull0 + 8u * bb);
     }
-    if (ok && Tn > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_ofinal(x), 0, ab));
+    if (ok && T > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_odone, (T - 1) & 1, ab));
       tc_fence_after();
     }
-    // All four warps of this warpgroup take the same branch.
-    ok = bar_and(1 + x, 128, ok && *abort_flag == 0);
-    if (ok && (x == 0 || hasB)) {
+    // All four softmax warps take the same branch: AND of every thread's ok.
+    ok = bar_and_128(1, ok && *abort_flag == 0);
+    if (ok) {
       // ---------------------------------------------------------- epilogue
       const float inv_l = lh_run > 0.f ? 1.f / lh_run : 0.f;
       if (grow < a.N) {
         const float Lv = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         a.L[static_cast<long long>(bh) * a.N + grow] = Lv;
       }
-      // O / l -> bf16 -> the (now idle) Q_X tile buffer, in the same swizzled
-      // layout TMA uses, then one TMA store per 64-column atom.  Every lane
-      // takes part in the warp-collective TMEM loads; TMA clips rows >= N.
-      const int qoff = C::kOffQ + x * C::kTileBytes;
+      // O / l -> bf16 -> the (now idle) Q tile buffer, in the same swizzled
+      // layout TMA uses, then one TMA store per 64-column atom.
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
-        if (Tn > 0) {
-          tmem_ld32(tl + ocol + 32 * c, o);
+        if (T > 0) {
+          tmem_ld32(tl + C::kColO + 32 * c, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -513,14 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           v.z = pack_bf16(__uint_as_float(o[8 * t + 4]) * inv_l, __uint_as_float(o[8 * t + 5]) * inv_l);
           v.w = pack_bf16(__uint_as_float(o[8 * t + 6]) * inv_l, __uint_as_float(o[8 * t + 7]) * inv_l);
           const int phys = (chunk0 + t) ^ (row & 7);
-          *reinterpret_cast<uint4*>(smem + qoff + atom * C::kAtomBytes + row * 128 + phys * 16) = v;
+          *reinterpret_cast<uint4*>(smem + C::kOffQ + atom * C::kAtomBytes + row * 128 + phys * 16) = v;
         }
       }
       fence_proxy_async_smem();
-      bar_sync(1 + x, 128);
-      if (quarter == 0 && lane == 0) {
-        for (int c = 0; c < C::kAtoms; ++c)
-          tma_store_3d(&tmO, sQ + x * C::kTileBytes + c * C::kAtomBytes, c * 64, q0, bh);
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (warp == 2 && lane == 0) {
+        for (int c = 0; c < C::kAtoms; ++c) tma_store_3d(&tmO, sQ + c * C::kAtomBytes, c * 64, q0, bh);
         bulk_commit();
         bulk_wait0();
       }
@@ -535,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD, bool DROP>
+template <int HD, bool DROP, bool MASKX>
 cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          const CUtensorMap& tmO, const FwdArgs& a, cudaStream_t stream) {
   using C = Cfg<HD>;
@@ -544,40 +513,40 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    // The register split (setmaxnreg) must fit in what the launch provides,
-    // or the increasing warpgroups would wait for registers forever.
-    cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, fa_fwd_kernel<HD, DROP>);
-    if (e != cudaSuccess) return e;
-    if (fattr.numRegs * kThreads < 128 * kRegsLow<DROP> + 256 * kRegsHigh<DROP>)
-      return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(fa_fwd_kernel<HD, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_fwd_1q_kernel<HD, DROP, MASKX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const long long grid = static_cast<long long>((a.n_qtiles + 1) / 2) * a.BH;
+  const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
+  fa_fwd_1q_kernel<HD, DROP, MASKX><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
                                                                                     tmO, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+template <int HD>
+cudaError_t launch_fwd_d(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
+                            cudaStream_t stream) {
+  const bool maskx = a.window >= 0 || a.bmask != nullptr;
+  if (a.drop_thr)
+    return maskx ? launch_fwd_t<HD, true, true>(tmQ, tmK, tmV, tmO, a, stream)
+                 : launch_fwd_t<HD, true, false>(tmQ, tmK, tmV, tmO, a, stream);
+  return maskx ? launch_fwd_t<HD, false, true>(tmQ, tmK, tmV, tmO, a, stream)
+               : launch_fwd_t<HD, false, false>(tmQ, tmK, tmV, tmO, a, stream);
+}
+
 cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
-                       cudaStream_t stream) {
-  if (fwd_one_block(d, a.window, a.bmask, a.drop_thr))
-    return launch_fwd_1q(d, tmQ, tmK, tmV, tmO, a, stream);
+                          const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
+                          cudaStream_t stream) {
   switch (d) {
-    case 64:
-      return a.drop_thr ? launch_fwd_t<64, true>(tmQ, tmK, tmV, tmO, a, stream)
-                        : launch_fwd_t<64, false>(tmQ, tmK, tmV, tmO, a, stream);
-    case 128:
-      return a.drop_thr ? launch_fwd_t<128, true>(tmQ, tmK, tmV, tmO, a, stream)
-                        : launch_fwd_t<128, false>(tmQ, tmK, tmV, tmO, a, stream);
+    case 64: return launch_fwd_d<64>(tmQ, tmK, tmV, tmO, a, stream);
+    case 128: return launch_fwd_d<128>(tmQ, tmK, tmV, tmO, a, stream);
+    case 256: return launch_fwd_d<256>(tmQ, tmK, tmV, tmO, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -24,26 +24,14 @@ struct FwdArgs {
   float out_scale;      // factor applied to O (e4m3 forward: V's dequantisation factor)
 };
 
-// Forward (dispatches between the two forward kernels, see fwd_one_block).
+// Forward (fa_fwd.cu): one 128-row query block per CTA and 64-key blocks
+// (the K and V maps use kFwdKvRows-row boxes), two CTAs per SM at d = 64 and
+// 128, one at d = 256; causal, key padding, window, block mask and dropout.
+// grid = ceil(N/128) * BH.
+constexpr int kFwdKvRows = 64;
 cudaError_t launch_fwd(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
                        cudaStream_t stream);
-
-// Forward with one 128-row query block per CTA and 64-key blocks (the K and
-// V maps use 64-row boxes), two CTAs per SM at d = 64 and 128, one at d = 256.
-// Causal and key padding only.  grid = ceil(N/128) * BH.
-cudaError_t launch_fwd_1q(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                          const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdArgs& a,
-                          cudaStream_t stream);
-// The forward kernel for a call: the one-block kernel unless a window, block
-// mask or dropout needs the two-block kernel of fa_fwd.cu.  (Measured on the
-// sweep, the one-block kernel with two CTAs per SM is 1.4-1.9x faster at
-// N <= 1024 and level at N = 16384, d = 128.)
-inline bool fwd_one_block(int d, int window, const void* bmask, uint32_t drop_thr) {
-  return d == 256 || (window < 0 && bmask == nullptr && drop_thr == 0);
-}
-// Rows of the K and V boxes of the kernel fwd_one_block picks.
-inline int fwd_kv_rows(bool one_block) { return one_block ? 64 : 128; }
 
 // e4m3 forward, d = 128 (fa_fwd_fp8.cu): V [BH, N, 128] -> V^T [BH, 128,
 // Npad] (Npad = N rounded up to 16, zero-filled), then the forward with Q, K

@@ -103,11 +103,11 @@ def test_block_sparse_empty_rows_window_and_padding(d):
 @pytest.mark.parametrize("causal", [False, True])
 def test_masks_that_change_nothing_change_nothing(d, causal):
     # An all-ones block mask, and a window wider than the sequence (with the
-    # causal term it implies), keep every pair.  The forward then runs on the
-    # two-block kernel instead of the one-block one (a different summation
-    # order: agreement to a few bf16 ulps); the backward kernels visit the
-    # same tiles with the same element masks: given the same O and L they
-    # agree bit for bit.
+    # causal term it implies), keep every pair.  The forward then runs the
+    # kernel instantiation with the window and block-mask terms (same tiles,
+    # same order; held to a few bf16 ulps, not bitwise, since the two are
+    # compiled separately); the backward kernels visit the same tiles with
+    # the same element masks: given the same O and L they agree bit for bit.
     from exact_io_aware_40_gb300 import fa
     N = 777
     case = H.Case(1501, 1, 3, N, d)
