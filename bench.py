@@ -60,10 +60,10 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
 # launches), valid only while the kernel source hashes to the recorded digest.
 # Capture: H=8 (same kernels, half the heads, inputs still larger than L2),
-# 135.3 MB read + 32.2 MB written (causal 0) and 135.4 + 27.8 MB (causal 1);
+# 135.3 MB read + 31.9 MB written (causal 0) and 135.5 + 23.9 MB (causal 1);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "a3eb85a39990c4f660320d7f2c88263dff914aa0dc39d8b973cd7bbd9393c181",
-                    "bytes_per_launch": 2 * (167.6e6 + 163.2e6) / 2}
+BWD_DKDV_TRAFFIC = {"sha256": "a3442fd30b8ca8356d65fce402b8bde9944d49c6d9d7186ccdfd547273c0a806",
+                    "bytes_per_launch": 2 * (167.27e6 + 159.35e6) / 2}
 
 
 def pairs(causal, b=None, h=None, n=None):
@@ -91,6 +91,53 @@ def job_throughput(flops_per_rank_step, world, ms_per_step):
     """Whole-job TFLOP/s: every rank runs the same step (independent replicas),
     so the job does world x the FLOPs of one rank in the slowest rank's time."""
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
+def timed_e2e(torch, stream, h2d, d2h, compute, n_steps):
+    """Milliseconds per step of a run of n_steps end-to-end steps, each one the
+    host -> device copy of its inputs, its kernels and the device -> host copy
+    of its results.  Step s uses device buffer set s % 2: h2d[i] lists the
+    (device, pinned host) input pairs of set i, d2h[i] the (pinned host,
+    device) result pairs, compute(i) enqueues the kernels on `stream`.  The
+    input copy of step s + 1 and the result copy of step s - 1 run on their
+    own streams while step s computes; every copy of every step lies between
+    the start and stop events."""
+    up, down = torch.cuda.Stream(stream.device), torch.cuda.Stream(stream.device)
+    loaded = [torch.cuda.Event() for _ in range(n_steps)]
+    computed = [torch.cuda.Event() for _ in range(n_steps)]
+    drained = [torch.cuda.Event() for _ in range(n_steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    up.wait_event(start)
+    down.wait_event(start)
+
+    def load(s):
+        if s >= 2:
+            up.wait_event(computed[s - 2])  # the set's inputs are no longer read
+        with torch.cuda.stream(up):
+            for dst, src in h2d[s % 2]:
+                dst.copy_(src, non_blocking=True)
+        loaded[s].record(up)
+
+    load(0)
+    for s in range(n_steps):
+        if s + 1 < n_steps:
+            load(s + 1)
+        stream.wait_event(loaded[s])
+        if s >= 2:
+            stream.wait_event(drained[s - 2])  # the set's results are copied out
+        compute(s % 2)
+        computed[s].record(stream)
+        down.wait_event(computed[s])
+        with torch.cuda.stream(down):
+            for dst, src in d2h[s % 2]:
+                dst.copy_(src, non_blocking=True)
+        drained[s].record(down)
+    stream.wait_event(drained[n_steps - 1])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / n_steps
 
 
 def load_peaks():
@@ -311,23 +358,31 @@ def run_masked(args, rank, world):
     bits = workload_bits()
     host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
             for k, v in bits.items()}
-    q, k, v, do = (host[n].to(dev) for n in ("Q", "K", "V", "dO"))
     bm_dev = None if bm is None else torch.from_numpy(bm).to(dev)
-    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
-    L = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    # two buffer sets (the end-to-end run alternates them); the device-resident
+    # timed region uses set 0
+    bufs = []
+    for _ in range(2):
+        t = {n: host[n].to(dev) for n in ("Q", "K", "V", "dO")}
+        for n in ("O", "dQ", "dK", "dV"):
+            t[n] = torch.empty_like(t["Q"])
+        t["L"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        bufs.append(t)
     ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
-    def step(ev=None):
+    def step(ev=None, b=0):
+        t = bufs[b]
+        q, k, v, do = t["Q"], t["K"], t["V"], t["dO"]
         if ev is not None:
             ev[0].record(stream)
-        fa.fa_fwd_dropout(q, k, v, o, L, scale, causal, None, window, bm_dev, DROPOUT,
+        fa.fa_fwd_dropout(q, k, v, t["O"], t["L"], scale, causal, None, window, bm_dev, DROPOUT,
                           DROPOUT_SEED, stream=sp)
         if ev is not None:
             ev[1].record(stream)
-        fa.fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, None, window, bm_dev,
-                          DROPOUT, DROPOUT_SEED, ws, stream=sp)
+        fa.fa_bwd_dropout(q, k, v, t["O"], do, t["L"], t["dQ"], t["dK"], t["dV"], scale, causal,
+                          None, window, bm_dev, DROPOUT, DROPOUT_SEED, ws, stream=sp)
         if ev is not None:
             ev[2].record(stream)
 
@@ -366,33 +421,22 @@ def run_masked(args, rank, world):
     flops = 14 * D * P
     value = job_throughput(flops, world, ms_step)
 
-    host_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
-                for n, t in (("o", o), ("L", L), ("dq", dq), ("dk", dk), ("dv", dv))}
-    dev_out = {"o": o, "L": L, "dq": dq, "dk": dk, "dv": dv}
-    h2d = sum(host[n].numel() * host[n].element_size() for n in ("Q", "K", "V", "dO"))
+    outs = ("O", "L", "dQ", "dK", "dV")
+    host_out = {n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory()
+                for n in outs}
+    ins = ("Q", "K", "V", "dO")
+    h2d_pairs = [[(bufs[b][n], host[n]) for n in ins] for b in (0, 1)]
+    d2h_pairs = [[(host_out[n], bufs[b][n]) for n in outs] for b in (0, 1)]
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    e2e_steps = max(1, min(args.steps, 10))
-
-    def e2e_step():
-        for dst, nm in ((q, "Q"), (k, "K"), (v, "V"), (do, "dO")):
-            dst.copy_(host[nm], non_blocking=True)
-        step()
-        for n in host_out:
-            host_out[n].copy_(dev_out[n], non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 10))
+    compute = lambda b: step(None, b)
+    timed_e2e(torch, stream, h2d_pairs, d2h_pairs, compute, 2)  # warm-up
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_e2e = timed_e2e(torch, stream, h2d_pairs, d2h_pairs, compute, e2e_steps)
     barrier()
     fa.fa_check_error(sp)
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    ms_e2e = max_over_ranks(ms_e2e, world, dev)
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -448,19 +492,24 @@ def run_fp8(args, rank, world):
     scale = 1.0 / math.sqrt(D)
     host = {n: torch.from_numpy(inputs.normal_e4m3_bits(SEED, inputs.STREAM[n], (B, H, N, D)))
             .pin_memory() for n in ("Q", "K", "V")}
-    q, k, v = (host[n].to(dev) for n in ("Q", "K", "V"))
-    out = {c: (torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev),
-               torch.empty((B, H, N), dtype=torch.float32, device=dev)) for c in (0, 1)}
+    # two buffer sets (the end-to-end run alternates them); the device-resident
+    # timed region uses set 0
+    ins = [{n: host[n].to(dev) for n in ("Q", "K", "V")} for _ in range(2)]
+    outs = [{c: (torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev),
+                 torch.empty((B, H, N), dtype=torch.float32, device=dev)) for c in (0, 1)}
+            for _ in range(2)]
+    out = outs[0]
     ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
-    def step(ev=None):
+    def step(ev=None, b=0):
+        q, k, v = ins[b]["Q"], ins[b]["K"], ins[b]["V"]
         for c in (0, 1):
             if ev is not None:
                 ev[c][0].record(stream)
-            fa.fa_fwd_fp8(q, k, v, out[c][0], out[c][1], scale, 1.0, 1.0, 1.0, c, None, ws,
-                          stream=sp)
+            fa.fa_fwd_fp8(q, k, v, outs[b][c][0], outs[b][c][1], scale, 1.0, 1.0, 1.0, c, None,
+                          ws, stream=sp)
             if ev is not None:
                 ev[c][1].record(stream)
 
@@ -501,27 +550,17 @@ def run_fp8(args, rank, world):
                     torch.empty(out[c][1].shape, dtype=torch.float32).pin_memory()) for c in (0, 1)}
     h2d = sum(host[n].numel() for n in ("Q", "K", "V"))
     d2h = sum(t.numel() * t.element_size() for c in (0, 1) for t in host_out[c])
-    e2e_steps = max(1, min(args.steps, 10))
-
-    def e2e_step():
-        for dst, nm in ((q, "Q"), (k, "K"), (v, "V")):
-            dst.copy_(host[nm], non_blocking=True)
-        step()
-        for c in (0, 1):
-            host_out[c][0].copy_(out[c][0], non_blocking=True)
-            host_out[c][1].copy_(out[c][1], non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 10))
+    h2d_pairs = [[(ins[b][n], host[n]) for n in ("Q", "K", "V")] for b in (0, 1)]
+    d2h_pairs = [[(host_out[c][i], outs[b][c][i]) for c in (0, 1) for i in (0, 1)]
+                 for b in (0, 1)]
+    compute = lambda b: step(None, b)
+    timed_e2e(torch, stream, h2d_pairs, d2h_pairs, compute, 2)  # warm-up
+    barrier()
+    ms_e2e = timed_e2e(torch, stream, h2d_pairs, d2h_pairs, compute, e2e_steps)
+    barrier()
     fa.fa_check_error(sp)
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    ms_e2e = max_over_ranks(ms_e2e, world, dev)
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -650,19 +689,26 @@ def run_ours(args, rank, world):
     bits = workload_bits()
     host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
             for k, v in bits.items()}
-    q, k, v, do = (host[n].to(dev) for n in ("Q", "K", "V", "dO"))
-    out = {}
-    for c in (0, 1):
-        out[c] = dict(o=torch.empty_like(q), L=torch.empty((B, H, N), dtype=torch.float32, device=dev),
-                      dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q))
+    # two buffer sets (the end-to-end run alternates them); the device-resident
+    # timed region uses set 0
+    ins, outs = [], []
+    for _ in range(2):
+        ins.append({n: host[n].to(dev) for n in ("Q", "K", "V", "dO")})
+        q = ins[-1]["Q"]
+        outs.append({c: dict(o=torch.empty_like(q),
+                             L=torch.empty((B, H, N), dtype=torch.float32, device=dev),
+                             dq=torch.empty_like(q), dk=torch.empty_like(q),
+                             dv=torch.empty_like(q)) for c in (0, 1)})
+    out = outs[0]
     ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     stages = ("fwd", "prep", "dkdv", "dq")
 
-    def step(ev=None):
+    def step(ev=None, b=0):
+        q, k, v, do = (ins[b][n] for n in ("Q", "K", "V", "dO"))
         for c in (0, 1):
-            t = out[c]
+            t = outs[b][c]
             if ev is not None:
                 ev[c][0].record(stream)
             fa.fa_fwd(q, k, v, t["o"], t["L"], scale, c, stream=sp)
@@ -725,29 +771,16 @@ def run_ours(args, rank, world):
                     for n in ("o", "L", "dq", "dk", "dv")} for c in (0, 1)}
     h2d = sum(host[n].numel() * host[n].element_size() for n in ("Q", "K", "V", "dO"))
     d2h = sum(t.numel() * t.element_size() for c in (0, 1) for t in host_out[c].values())
-    e2e_steps = max(1, min(args.steps, 10))
-
-    def e2e_step():
-        for dst, nm in ((q, "Q"), (k, "K"), (v, "V"), (do, "dO")):
-            dst.copy_(host[nm], non_blocking=True)
-        step()
-        for c in (0, 1):
-            for n in ("o", "L", "dq", "dk", "dv"):
-                host_out[c][n].copy_(out[c][n], non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 10))
+    h2d_pairs = [[(ins[b][n], host[n]) for n in ("Q", "K", "V", "dO")] for b in (0, 1)]
+    d2h_pairs = [[(host_out[c][n], outs[b][c][n]) for c in (0, 1)
+                  for n in ("o", "L", "dq", "dk", "dv")] for b in (0, 1)]
+    compute = lambda b: step(None, b)
+    timed_e2e(torch, stream, h2d_pairs, d2h_pairs, compute, 2)  # warm-up
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_e2e = timed_e2e(torch, stream, h2d_pairs, d2h_pairs, compute, e2e_steps)
     barrier()
     fa.fa_check_error(sp)
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
     ms_e2e = max_over_ranks(ms_e2e, world, dev)
 
     if rank != 0:
