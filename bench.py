@@ -60,10 +60,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
 # launches), valid only while the kernel source hashes to the recorded digest.
 # Capture: H=8 (same kernels, half the heads, inputs still larger than L2),
-# 135.3 MB read + 31.9 MB written (causal 0) and 135.5 + 23.9 MB (causal 1);
+# 135.5 MB read + 32.0 MB written (causal 0) and 154.0 + 22.5 MB (causal 1;
+# the grouped CTA order of a causal launch re-reads some Q, dO blocks);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "a3442fd30b8ca8356d65fce402b8bde9944d49c6d9d7186ccdfd547273c0a806",
-                    "bytes_per_launch": 2 * (167.27e6 + 159.35e6) / 2}
+BWD_DKDV_TRAFFIC = {"sha256": "8a760372259f15ee97238b5db690edb5a8f5347c698f9e6bf0788546eee07ad3",
+                    "bytes_per_launch": 2 * (167.45e6 + 176.50e6) / 2}
 
 
 def pairs(causal, b=None, h=None, n=None):

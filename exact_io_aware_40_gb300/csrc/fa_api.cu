@@ -12,6 +12,21 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+namespace fa {
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace fa
+
 namespace {
 
 // One error word per device, written by kernels that give up on a stalled
@@ -232,6 +247,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.seed_hi = drop.seed_hi;
   a.drop_scale = drop.scale;
   a.out_scale = 1.f;
+  a.tile_group = a.n_qtiles;  // the launcher picks the CTA order
   if (fa::launch_fwd(d, tq, tk, tv, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -317,6 +333,7 @@ fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float
   a.nb = a.n_qtiles;
   a.drop_scale = 1.f;
   a.out_scale = descale_v;
+  a.tile_group = a.n_qtiles;  // the launcher picks the CTA order
   if (fa::launch_transpose_v8(V, workspace, BH, N, npad, stream) != cudaSuccess)
     return FA_ERR_CUDA;
   if (fa::launch_fwd_fp8(tq, tk, tvt, to, a, stream) != cudaSuccess) return FA_ERR_CUDA;
@@ -392,6 +409,7 @@ static fa_status bwd_args(const void* Q, const void* K, const void* V, const voi
   a->seed_lo = drop.seed_lo;
   a->seed_hi = drop.seed_hi;
   a->drop_scale = drop.scale;
+  a->tile_group = a->n_ktiles;  // the launchers pick the CTA order
   return FA_OK;
 }
 

@@ -130,9 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Head-major order; small kt (most work under causal) first.
-  const int bh = static_cast<int>(blockIdx.x / a.n_ktiles);
-  const int kt = static_cast<int>(blockIdx.x % a.n_ktiles);
+  // Small kt (most work under causal) first, in groups of ranks, head-major
+  // inside a group.
+  int bh, kt;
+  cta_tile(static_cast<int>(blockIdx.x), a.n_ktiles, a.BH, a.tile_group, &bh, &kt);
   const int k0 = kt * kT;
   const int b = bh / a.H;
   int kv_limit = a.N;
@@ -514,9 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Head-major order with the longest query blocks (causal) of a head first.
-  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
+  // Longest query blocks (causal) first, in groups of ranks, head-major inside
+  // a group.
+  int bh, qt;
+  cta_tile(static_cast<int>(blockIdx.x), a.n_qtiles, a.BH, a.tile_group, &bh, &qt);
+  qt = a.n_qtiles - 1 - qt;
   const int q0 = qt * kT;
   const int b = bh / a.H;
   int kv_limit = a.N;
@@ -829,8 +832,11 @@ cudaError_t launch_dkdv_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const 
   const long long grid = static_cast<long long>(a.n_ktiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  BwdArgs ag = a;
+  ag.tile_group = tile_group(a.causal != 0, a.n_ktiles, a.BH, 1,
+                             4ll * a.N * HD);  // Q and dO of a head, bf16
   fa_bwd_dkdv_wide_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, KvW<HD>::kSmemBytes,
-                                stream>>>(tmQ, tmK, tmV, tmdO, a);
+                                stream>>>(tmQ, tmK, tmV, tmdO, ag);
   return cudaGetLastError();
 }
 
@@ -844,8 +850,11 @@ cudaError_t launch_dq_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CU
   const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  BwdArgs ag = a;
+  ag.tile_group = tile_group(a.causal != 0, a.n_qtiles, a.BH, 1,
+                             4ll * a.N * HD);  // K and V of a head, bf16
   fa_bwd_dq_wide_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, QW<HD>::kSmemBytes,
-                              stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, a);
+                              stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, ag);
   return cudaGetLastError();
 }
 

@@ -127,10 +127,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // Head-major order: the CTAs in flight share one head's K/V (L2 reuse); within
-  // a head the longest query blocks (causal) start first.
-  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
+  // Longest query blocks (causal) first, in groups of ranks, head-major inside
+  // a group: the CTAs in flight share a few K/V blocks per head in L2.
+  int bh, qt;
+  cta_tile(static_cast<int>(blockIdx.x), a.n_qtiles, a.BH, a.tile_group, &bh, &qt);
+  qt = a.n_qtiles - 1 - qt;
   const int q0 = qt * kBR;
   const int b = bh / a.H;
   int kv_limit = a.N;
@@ -521,8 +522,11 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  FwdArgs ag = a;
+  ag.tile_group = tile_group(a.causal != 0, a.n_qtiles, a.BH, C::kMinBlocks,
+                             4ll * a.N * HD);  // K and V of a head, bf16
   fa_fwd_1q_kernel<HD, DROP, MASKX><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
-                                                                                    tmO, a);
+                                                                                    tmO, ag);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@
 #include <type_traits>
 
 #include "kernels.h"
+#include "masks.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -103,9 +104,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // Head-major order; within a head the longest query blocks (causal) first.
-  const int bh = static_cast<int>(blockIdx.x / a.n_qtiles);
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.x % a.n_qtiles);
+  // Longest query blocks (causal) first, in groups of ranks, head-major inside
+  // a group.
+  int bh, qt;
+  cta_tile(static_cast<int>(blockIdx.x), a.n_qtiles, a.BH, a.tile_group, &bh, &qt);
+  qt = a.n_qtiles - 1 - qt;
   const int q0 = qt * kBR;
   const int b = bh / a.H;
   int kv_limit = a.N;
@@ -433,8 +436,11 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& tmQ, const CUtensorMap& tmK, const
   const long long grid = static_cast<long long>(a.n_qtiles) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  FwdArgs ag = a;
+  // 512 TMEM columns: one CTA per SM; K and V^T of a head, e4m3
+  ag.tile_group = tile_group(a.causal != 0, a.n_qtiles, a.BH, 1, 2ll * a.N * 128);
   fa_fwd_fp8_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tmQ, tmK, tmVt,
-                                                                                 tmO, a);
+                                                                                 tmO, ag);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,26 @@ struct FwdArgs {
   uint32_t seed_lo, seed_hi;
   float drop_scale;     // 65536 / (65536 - drop_thr)
   float out_scale;      // factor applied to O (e4m3 forward: V's dequantisation factor)
+  int tile_group;       // CTA order (cta_tile in masks.cuh); set by the launcher
 };
+
+// Multiprocessors of the current device (cached per device; 0 on error).
+int sm_count();
+
+// Group width for cta_tile.  Only a causal mask gives the CTAs of a launch
+// very different amounts of work (the longest tile has n_tiles times the
+// shortest's); then one group of all BH heads should about fill the resident
+// CTAs (ctas_per_sm x SMs).  Otherwise plain head-major order.  With a width
+// of 1 the CTAs of a head in flight share no reads, so that order pays only
+// while the operands every CTA of a head streams (head_bytes per head) stay
+// in L2 for all heads: a 2048-token, 128-head d = 128 backward (128 MB of
+// Q and dO) ran 8 % slower tile-major; 96 heads of 1024 x 64 (25 MB) gained.
+inline int tile_group(bool causal, int n_tiles, int BH, int ctas_per_sm, long long head_bytes) {
+  if (!causal || BH <= 0) return n_tiles;
+  const int g = ctas_per_sm * sm_count() / BH;
+  if (g >= 2) return g > n_tiles ? n_tiles : g;
+  return static_cast<long long>(BH) * head_bytes <= (32ll << 20) ? 1 : n_tiles;
+}
 
 // Forward (fa_fwd.cu): one 128-row query block per CTA and 64-key blocks
 // (the K and V maps use kFwdKvRows-row boxes), two CTAs per SM at d = 64 and
@@ -70,6 +89,7 @@ struct BwdArgs {
   uint32_t drop_thr;    // dropout: 0 = none, else floor(p * 65536)
   uint32_t seed_lo, seed_hi;
   float drop_scale;     // 65536 / (65536 - drop_thr)
+  int tile_group;       // CTA order (cta_tile in masks.cuh); set by the launcher
 };
 
 // Query rows per step of the dK/dV kernel (the box height of its Q and dO

@@ -73,6 +73,24 @@ __device__ __forceinline__ int count_blocks(const uint8_t* m, int stride, int lo
   return n;
 }
 
+// The (batch-head, tile rank) a CTA owns.  Ranks are taken in groups of
+// `group` consecutive ranks, rank 0 first, and head-major inside a group;
+// group >= n_tiles is plain head-major order.  Rank 0 is the tile with the
+// most work under a causal mask: when one group of all heads about fills the
+// GPU's resident CTAs, the longest tiles of every head start in the first
+// waves instead of the last head's starting near the end of the grid, and
+// the CTAs of one head in a group still walk K/V (or Q/dO) side by side.
+__device__ __forceinline__ void cta_tile(int cta, int n_tiles, int BH, int group, int* bh,
+                                         int* rank) {
+  const int w_full = max(1, min(group, n_tiles));
+  const int g = cta / (w_full * BH);
+  const int first = g * w_full;                // first rank of the group
+  const int w = min(w_full, n_tiles - first);  // ranks in this group
+  const int r = cta - first * BH;
+  *bh = r / w;
+  *rank = first + r % w;
+}
+
 // Element mask inside a tile: is key `key` visible from query `row`?
 __device__ __forceinline__ bool visible(int row, int key, int kv_limit, int causal, int window) {
   const bool band = (causal != 0) | (window >= 0);
