@@ -833,7 +833,7 @@ cudaError_t launch_dkdv_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const 
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   BwdArgs ag = a;
-  ag.tile_group = tile_group(a.causal != 0, a.n_ktiles, a.BH, 1,
+  ag.tile_group = tile_group(a.causal != 0 && a.window < 0, a.n_ktiles, a.BH, 1,
                              4ll * a.N * HD);  // Q and dO of a head, bf16
   fa_bwd_dkdv_wide_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, KvW<HD>::kSmemBytes,
                                 stream>>>(tmQ, tmK, tmV, tmdO, ag);
@@ -851,7 +851,7 @@ cudaError_t launch_dq_w(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CU
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   BwdArgs ag = a;
-  ag.tile_group = tile_group(a.causal != 0, a.n_qtiles, a.BH, 1,
+  ag.tile_group = tile_group(a.causal != 0 && a.window < 0, a.n_qtiles, a.BH, 1,
                              4ll * a.N * HD);  // K and V of a head, bf16
   fa_bwd_dq_wide_kernel<HD, DROP><<<static_cast<unsigned>(grid), kThreads, QW<HD>::kSmemBytes,
                               stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, ag);

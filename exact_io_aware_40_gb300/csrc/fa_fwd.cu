@@ -523,7 +523,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   FwdArgs ag = a;
-  ag.tile_group = tile_group(a.causal != 0, a.n_qtiles, a.BH, C::kMinBlocks,
+  ag.tile_group = tile_group(a.causal != 0 && a.window < 0, a.n_qtiles, a.BH, C::kMinBlocks,
                              4ll * a.N * HD);  // K and V of a head, bf16
   fa_fwd_1q_kernel<HD, DROP, MASKX><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV,
                                                                                     tmO, ag);

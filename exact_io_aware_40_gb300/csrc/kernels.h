@@ -28,14 +28,15 @@ struct FwdArgs {
 // Multiprocessors of the current device (cached per device; 0 on error).
 int sm_count();
 
-// Group width for cta_tile.  Only a causal mask gives the CTAs of a launch
-// very different amounts of work (the longest tile has n_tiles times the
-// shortest's); then one group of all BH heads should about fill the resident
-// CTAs (ctas_per_sm x SMs).  Otherwise plain head-major order.  With a width
-// of 1 the CTAs of a head in flight share no reads, so that order pays only
-// while the operands every CTA of a head streams (head_bytes per head) stay
-// in L2 for all heads: a 2048-token, 128-head d = 128 backward (128 MB of
-// Q and dO) ran 8 % slower tile-major; 96 heads of 1024 x 64 (25 MB) gained.
+// Group width for cta_tile.  Only a causal mask without a window gives the
+// CTAs of a launch very different amounts of work (the longest tile has
+// n_tiles times the shortest's; a window makes them about equal); then one
+// group of all BH heads should about fill the resident CTAs (ctas_per_sm x
+// SMs).  Otherwise plain head-major order.  With a width of 1 the CTAs of a
+// head in flight share no reads, so that order pays only while the operands
+// every CTA of a head streams (head_bytes per head) stay in L2 for all
+// heads: a 2048-token, 128-head d = 128 backward (128 MB of Q and dO) ran
+// 8 % slower tile-major; 96 heads of 1024 x 64 (25 MB) gained.
 inline int tile_group(bool causal, int n_tiles, int BH, int ctas_per_sm, long long head_bytes) {
   if (!causal || BH <= 0) return n_tiles;
   const int g = ctas_per_sm * sm_count() / BH;
@@ -79,7 +80,7 @@ struct BwdArgs {
   int* err;
   int H, N, BH;
   int n_ktiles;         // ceil(N / 128): key blocks of the dK/dV kernel
-  int n_qtiles;         // query steps: ceil(N / 64) for dK/dV, ceil(N / 128) for dQ
+  int n_qtiles;         // query steps: ceil(N / bwd_dkdv_qrows(d)) for dK/dV, ceil(N / 128) for dQ
   float scale;          // softmax scale
   float scale_log2;     // scale * log2(e)
   int causal;
