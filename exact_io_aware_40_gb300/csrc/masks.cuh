@@ -80,12 +80,14 @@ __device__ __forceinline__ int count_blocks(const uint8_t* m, int stride, int lo
 // GPU's resident CTAs, the longest tiles of every head start in the first
 // waves instead of the last head's starting near the end of the grid, and
 // the CTAs of one head in a group still walk K/V (or Q/dO) side by side.
-__device__ __forceinline__ void cta_tile(int cta, int n_tiles, int BH, int group, int* bh,
-                                         int* rank) {
-  const int w_full = max(1, min(group, n_tiles));
+__host__ __device__ __forceinline__ void cta_tile(int cta, int n_tiles, int BH, int group,
+                                                  int* bh, int* rank) {
+  int w_full = group < n_tiles ? group : n_tiles;
+  if (w_full < 1) w_full = 1;
   const int g = cta / (w_full * BH);
-  const int first = g * w_full;                // first rank of the group
-  const int w = min(w_full, n_tiles - first);  // ranks in this group
+  const int first = g * w_full;  // first rank of the group
+  const int left = n_tiles - first;
+  const int w = w_full < left ? w_full : left;  // ranks in this group
   const int r = cta - first * BH;
   *bh = r / w;
   *rank = first + r % w;
