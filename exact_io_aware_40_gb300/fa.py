@@ -251,6 +251,12 @@ def fa_check_error(stream=None, device=None):
 MASK_BLOCK = 128  # block size of block_mask (FA_MASK_BLOCK)
 
 
+def _same_device(*ts):
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) > 1:
+        raise ValueError("all tensors must be on one CUDA device, got %s" % sorted(map(str, devs)))
+
+
 def _expect_mask(block_mask, N):
     import torch
     if block_mask is not None:
@@ -272,19 +278,23 @@ def attention_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, lse=
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
+    _expect(out, "out", torch.bfloat16, (B, H, N, d))
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _expect(lse, "lse", torch.float32, (B, H, N))
     if kv_len is not None:
         _expect(kv_len, "kv_len", torch.int32, (B,))
-    if dropout_p > 0.0:
-        _expect_mask(block_mask, N)
-        fa_fwd_dropout(q, k, v, out, lse, scale, causal, kv_len, window, block_mask, dropout_p,
-                       seed, stream)
-    elif window >= 0 or block_mask is not None:
-        _expect_mask(block_mask, N)
-        fa_fwd_masked(q, k, v, out, lse, scale, causal, kv_len, window, block_mask, stream)
-    else:
-        fa_fwd_kvlen(q, k, v, out, lse, scale, causal, kv_len, stream)
+    _same_device(q, k, v, out, lse, kv_len, block_mask)
+    with torch.cuda.device(q.device):
+        if dropout_p > 0.0:
+            _expect_mask(block_mask, N)
+            fa_fwd_dropout(q, k, v, out, lse, scale, causal, kv_len, window, block_mask,
+                           dropout_p, seed, stream)
+        elif window >= 0 or block_mask is not None:
+            _expect_mask(block_mask, N)
+            fa_fwd_masked(q, k, v, out, lse, scale, causal, kv_len, window, block_mask, stream)
+        else:
+            fa_fwd_kvlen(q, k, v, out, lse, scale, causal, kv_len, stream)
     return out, lse
 
 
@@ -303,15 +313,18 @@ def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, work
     need = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _expect(workspace, "workspace", torch.uint8, (workspace.numel(),))
+    _same_device(q, k, v, o, do, L, kv_len, block_mask, workspace)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    if dropout_p > 0.0:
-        _expect_mask(block_mask, N)
-        fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
-                       dropout_p, seed, workspace, stream)
-    elif window >= 0 or block_mask is not None:
-        _expect_mask(block_mask, N)
-        fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window, block_mask,
-                      workspace, stream)
-    else:
-        fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream)
+    with torch.cuda.device(q.device):
+        if dropout_p > 0.0:
+            _expect_mask(block_mask, N)
+            fa_bwd_dropout(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window,
+                           block_mask, dropout_p, seed, workspace, stream)
+        elif window >= 0 or block_mask is not None:
+            _expect_mask(block_mask, N)
+            fa_bwd_masked(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, window,
+                          block_mask, workspace, stream)
+        else:
+            fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream)
     return dq, dk, dv

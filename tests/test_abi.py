@@ -147,3 +147,17 @@ def test_fp8_entry_point_validates_on_the_host(lib):
     assert call(128, 0.0, 1 << 20) == 1         # descale factor must be > 0
     assert call(128, float("inf"), 1 << 20) == 1
     assert call(128, 1.0, 64) == 1              # short workspace
+
+
+def test_convenience_api_has_no_cpu_path():
+    # CPU tensors are refused before any call: there is no host fallback.
+    import torch
+    from exact_io_aware_40_gb300 import fa
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    L = torch.zeros(1, 2, 128, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.attention_fwd(q, q, q)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.attention_bwd(q, q, q, q, q, L)
+    with pytest.raises(ValueError, match="one CUDA device"):
+        fa._same_device(q, torch.zeros(1, device="meta"))
