@@ -328,3 +328,57 @@ def attention_bwd(q, k, v, o, do, L, causal=False, scale=None, kv_len=None, work
         else:
             fa_bwd(q, k, v, o, do, L, dq, dk, dv, scale, causal, kv_len, workspace, stream)
     return dq, dk, dv
+
+
+# ------------------------------------------------------------------ autograd
+
+_FLASH_FN = None
+
+
+def _flash_function():
+    """The torch.autograd.Function over attention_fwd / attention_bwd (built on
+    first use so that importing this module does not import torch)."""
+    global _FLASH_FN
+    if _FLASH_FN is None:
+        import torch
+
+        class FlashAttnFunction(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, causal, scale, kv_len, window, block_mask, dropout_p, seed):
+                o, L = attention_fwd(q, k, v, causal=causal, scale=scale, kv_len=kv_len,
+                                     window=window, block_mask=block_mask,
+                                     dropout_p=dropout_p, seed=seed)
+                ctx.save_for_backward(q, k, v, o, L)
+                ctx.rest = (causal, scale, kv_len, window, block_mask, dropout_p, seed)
+                ctx.mark_non_differentiable(L)
+                return o, L
+
+            @staticmethod
+            def backward(ctx, do, _dL):
+                q, k, v, o, L = ctx.saved_tensors
+                causal, scale, kv_len, window, block_mask, dropout_p, seed = ctx.rest
+                dq, dk, dv = attention_bwd(q, k, v, o, do.contiguous(), L, causal=causal,
+                                           scale=scale, kv_len=kv_len, window=window,
+                                           block_mask=block_mask, dropout_p=dropout_p, seed=seed)
+                return dq, dk, dv, None, None, None, None, None, None, None
+
+        _FLASH_FN = FlashAttnFunction
+    return _FLASH_FN
+
+
+def flash_attn_func(q, k, v, causal=False, softmax_scale=None, kv_len=None, window=-1,
+                    block_mask=None, dropout_p=0.0, seed=0, return_lse=False):
+    """Exact attention as a differentiable op: O = softmax(scale * Q K^T + mask) V.
+
+    The drop-in form of the method's interface (Q, K, V and a causal flag in,
+    the attention output out) with torch autograd: the backward runs
+    attention_bwd, recomputing P from the saved logsumexp L.  Tensors are
+    contiguous bf16 CUDA [B, H, N, d] (heads before tokens); softmax_scale
+    defaults to 1/sqrt(d); the mask and dropout arguments are those of
+    attention_fwd.  Returns O, or (O, L) with return_lse (L is not
+    differentiable)."""
+    d = q.shape[-1]
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    o, L = _flash_function().apply(q, k, v, bool(causal), scale, kv_len, int(window), block_mask,
+                                   float(dropout_p), int(seed))
+    return (o, L) if return_lse else o
