@@ -161,3 +161,39 @@ def test_convenience_api_has_no_cpu_path():
         fa.attention_bwd(q, q, q, q, q, L)
     with pytest.raises(ValueError, match="one CUDA device"):
         fa._same_device(q, torch.zeros(1, device="meta"))
+
+
+def _header_prototypes():
+    """name -> (return type, [parameter types]) for every function in include/*.h."""
+    protos = {}
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*((?:const\s+)?[A-Za-z_]\w*\s*\**)\s*(fa_\w+)\s*\(([^)]*)\)\s*;",
+                             text, flags=re.M):
+            params = [re.sub(r"\s*\b\w+$", "", p.strip()) for p in m.group(3).split(",")]
+            protos[m.group(2)] = (m.group(1).strip(), [p for p in params if p])
+    return protos
+
+
+def _ctype(c):
+    if "*" in c or c in ("fa_stream_t",):
+        return ctypes.c_void_p
+    return {"int": ctypes.c_int, "float": ctypes.c_float, "size_t": ctypes.c_size_t,
+            "uint64_t": ctypes.c_uint64, "fa_status": ctypes.c_int}[c]
+
+
+def test_binding_signatures_match_the_header(lib):
+    # A parameter the binding declares with the wrong type or position would
+    # hand the kernels a wrong pointer or size: every prototype is compared.
+    protos = _header_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert list(fn.argtypes) == [_ctype(p) for p in params], name
+        want_ret = {"fa_status": ctypes.c_int, "size_t": ctypes.c_size_t,
+                    "const char*": ctypes.c_char_p}[re.sub(r"\s+\*", "*", ret)]
+        assert fn.restype == want_ret, name
