@@ -102,8 +102,9 @@ def fake_torch(g, main):
 
 
 def run_pipeline(fn, n_steps):
-    """Run a timed_e2e-like function on fakes; returns (graph, main-stream
-    markers of start / stop, the copy and compute nodes)."""
+    """Run a timed_e2e-like function on fakes; returns the graph, the index
+    of the first node it created (the start event's record) and the nodes of
+    the compute calls."""
     g = Graph()
     main = FakeStream(g, "main")
     torch, cuda = fake_torch(g, main)
