@@ -482,7 +482,6 @@ def run_masked(args, rank, world):
 # ---------------------------------------------------------------- e4m3 forward
 
 def run_fp8(args, rank, world):
-    import numpy as np
     import torch
     import torch.distributed as dist
     from exact_io_aware_40_gb300 import build as fab, fa, inputs
@@ -681,7 +680,7 @@ def run_ours(args, rank, world):
     import numpy as np
     import torch
     import torch.distributed as dist
-    from exact_io_aware_40_gb300 import build as fab, fa, inputs
+    from exact_io_aware_40_gb300 import build as fab, fa
 
     fab.build()
     fa.load_library()

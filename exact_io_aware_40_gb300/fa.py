@@ -100,7 +100,6 @@ def _shape(q):
 
 
 def _expect(t, name, dtype, shape):
-    import torch
     if t is None:
         raise ValueError("%s is required" % name)
     if not t.is_cuda or t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != shape:
