@@ -309,10 +309,9 @@ typedef struct {
     int err;
 } fwd_ctx_t;
 
-static void fwd_task(void *vctx, int64_t bh, int worker)
+/* Rows of the panels first, first + stride, ... of head bh. */
+static void fwd_panels(fwd_ctx_t *c, int64_t bh, int64_t first, int64_t stride)
 {
-    (void)worker;
-    fwd_ctx_t *c = (fwd_ctx_t *)vctx;
     int64_t N = c->N;
     int d = c->d;
     int64_t b = bh / c->H;
@@ -330,7 +329,7 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
         free(s); free(p); free(lse);
         return;
     }
-    for (int64_t r0 = 0; r0 < N; r0 += R) {
+    for (int64_t r0 = first * R; r0 < N; r0 += stride * R) {
         int64_t rr = (r0 + R <= N) ? R : N - r0;
         panel_probs(q, k, N, d, c->scale, &msk, r0, rr, s, p, lse);
         for (int64_t r = 0; r < rr; ++r) {
@@ -350,6 +349,71 @@ static void fwd_task(void *vctx, int64_t bh, int worker)
     free(s); free(p); free(lse);
 }
 
+/* Split of the host threads: heads run in parallel; when there are fewer
+ * heads than threads, the row panels of one head are dealt out to a team of
+ * `inner` threads (panel t to team member t mod inner). */
+typedef struct {
+    void *ctx;
+    int64_t bh;
+    int64_t member, inner;
+    double *dk, *dv; /* backward: this member's partial dK, dV of the head */
+} team_arg_t;
+
+static void *fwd_member(void *arg)
+{
+    team_arg_t *t = (team_arg_t *)arg;
+    fwd_panels((fwd_ctx_t *)t->ctx, t->bh, t->member, t->inner);
+    return NULL;
+}
+
+/* Runs fn(args[0..n)) on n threads (member 0 on the calling thread). */
+static void run_team(void *(*fn)(void *), team_arg_t *args, int64_t n)
+{
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n);
+    int64_t started = 1;
+    if (th) {
+        for (; started < n; ++started)
+            if (pthread_create(&th[started], NULL, fn, &args[started]) != 0) break;
+    }
+    fn(&args[0]);
+    for (int64_t w = 1; w < started; ++w) pthread_join(th[w], NULL);
+    /* members whose thread could not be started run here, in order */
+    for (int64_t w = started; w < n; ++w) fn(&args[w]);
+    free(th);
+}
+
+typedef struct {
+    void *ctx;
+    int64_t inner;
+} outer_ctx_t;
+
+static void fwd_task(void *vctx, int64_t bh, int worker)
+{
+    (void)worker;
+    outer_ctx_t *oc = (outer_ctx_t *)vctx;
+    if (oc->inner <= 1) {
+        fwd_panels((fwd_ctx_t *)oc->ctx, bh, 0, 1);
+        return;
+    }
+    team_arg_t *ta = (team_arg_t *)calloc((size_t)oc->inner, sizeof(team_arg_t));
+    if (!ta) { ((fwd_ctx_t *)oc->ctx)->err = ORACLE_ERR_NOMEM; return; }
+    for (int64_t w = 0; w < oc->inner; ++w) {
+        ta[w].ctx = oc->ctx;
+        ta[w].bh = bh;
+        ta[w].member = w;
+        ta[w].inner = oc->inner;
+    }
+    run_team(fwd_member, ta, oc->inner);
+    free(ta);
+}
+
+/* Threads per head when there are fewer heads than threads. */
+static int64_t inner_threads(int64_t heads, int nthreads)
+{
+    if (heads < 1 || nthreads <= heads) return 1;
+    return nthreads / heads;
+}
+
 int oracle_attn_fwd(const double *q, const double *k, const double *v, int B, int H,
                     int N, int d, double scale, int causal, const int *kv_len, int window,
                     const unsigned char *block_mask, int block, double drop_p,
@@ -360,12 +424,14 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v, int B, in
     if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     fwd_ctx_t c = {q, k, v, H, N, d, scale, causal, kv_len, window, block_mask, block,
                    drop_p, seed, o, L, ORACLE_OK};
-    run_pool(fwd_task, &c, (int64_t)B * H, nthreads);
+    outer_ctx_t oc = {&c, inner_threads((int64_t)B * H, nthreads)};
+    run_pool(fwd_task, &oc, (int64_t)B * H, nthreads);
     return c.err;
 }
 
 /* ------------------------------------------------------------------------ */
-/* Backward over whole tensors (one task per (b, h): no cross-task sums).    */
+/* Backward over whole tensors (one task per (b, h); a head split across a   */
+/* team of threads sums the members' dK, dV partials in member order).       */
 
 typedef struct {
     const double *q, *k, *v, *dout;
@@ -383,10 +449,11 @@ typedef struct {
     int err;
 } bwd_ctx_t;
 
-static void bwd_task(void *vctx, int64_t bh, int worker)
+/* dQ rows of the panels first, first + stride, ... of head bh; their dK and
+ * dV contributions are added to dk_acc, dv_acc ([N, d] of that head). */
+static void bwd_panels(bwd_ctx_t *c, int64_t bh, int64_t first, int64_t stride,
+                       double *dk_acc, double *dv_acc)
 {
-    (void)worker;
-    bwd_ctx_t *c = (bwd_ctx_t *)vctx;
     int64_t N = c->N;
     int d = c->d;
     int64_t b = bh / c->H;
@@ -395,7 +462,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
     drop_t z = make_drop(c->drop_p, c->seed, b, bh % c->H);
     int64_t off = bh * N * d;
     const double *q = c->q + off, *k = c->k + off, *v = c->v + off, *dout = c->dout + off;
-    double *dq = c->dq + off, *dk = c->dk + off, *dv = c->dv + off;
+    double *dq = c->dq + off;
     int64_t R = panel_rows(N);
     double *s = (double *)malloc(sizeof(double) * (size_t)(R * N));
     double *p = (double *)malloc(sizeof(double) * (size_t)(R * N));
@@ -406,9 +473,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
         free(s); free(p); free(dp); free(lse);
         return;
     }
-    memset(dk, 0, sizeof(double) * (size_t)(N * d));
-    memset(dv, 0, sizeof(double) * (size_t)(N * d));
-    for (int64_t r0 = 0; r0 < N; r0 += R) {
+    for (int64_t r0 = first * R; r0 < N; r0 += stride * R) {
         int64_t rr = (r0 + R <= N) ? R : N - r0;
         panel_probs(q, k, N, d, c->scale, &msk, r0, rr, s, p, lse);
         for (int64_t r = 0; r < rr; ++r) {
@@ -430,7 +495,7 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
                 double pdij = pij * drop_mult(&z, i, j);
                 const double *kj = k + j * d;
                 const double *qi = q + i * d;
-                double *dkj = dk + j * d, *dvj = dv + j * d;
+                double *dkj = dk_acc + j * d, *dvj = dv_acc + j * d;
                 for (int c2 = 0; c2 < d; ++c2) {
                     dqi[c2] += c->scale * dsij * kj[c2];
                     dkj[c2] += c->scale * dsij * qi[c2];
@@ -440,6 +505,56 @@ static void bwd_task(void *vctx, int64_t bh, int worker)
         }
     }
     free(s); free(p); free(dp); free(lse);
+}
+
+static void *bwd_member(void *arg)
+{
+    team_arg_t *t = (team_arg_t *)arg;
+    bwd_panels((bwd_ctx_t *)t->ctx, t->bh, t->member, t->inner, t->dk, t->dv);
+    return NULL;
+}
+
+static void bwd_task(void *vctx, int64_t bh, int worker)
+{
+    (void)worker;
+    outer_ctx_t *oc = (outer_ctx_t *)vctx;
+    bwd_ctx_t *c = (bwd_ctx_t *)oc->ctx;
+    int64_t N = c->N;
+    int d = c->d;
+    int64_t off = bh * N * d;
+    double *dk = c->dk + off, *dv = c->dv + off;
+    memset(dk, 0, sizeof(double) * (size_t)(N * d));
+    memset(dv, 0, sizeof(double) * (size_t)(N * d));
+    if (oc->inner <= 1) {
+        bwd_panels(c, bh, 0, 1, dk, dv);
+        return;
+    }
+    /* Member 0 adds into dk, dv; the others into partials that are then
+     * added in member order (a fixed order: the result does not depend on
+     * thread timing). */
+    int64_t W = oc->inner;
+    team_arg_t *ta = (team_arg_t *)calloc((size_t)W, sizeof(team_arg_t));
+    double *part = (double *)calloc((size_t)(2 * (W - 1) * N * d), sizeof(double));
+    if (!ta || !part) {
+        free(ta); free(part);
+        c->err = ORACLE_ERR_NOMEM;
+        return;
+    }
+    for (int64_t w = 0; w < W; ++w) {
+        ta[w].ctx = c;
+        ta[w].bh = bh;
+        ta[w].member = w;
+        ta[w].inner = W;
+        ta[w].dk = w == 0 ? dk : part + (2 * (w - 1)) * N * d;
+        ta[w].dv = w == 0 ? dv : part + (2 * (w - 1) + 1) * N * d;
+    }
+    run_team(bwd_member, ta, W);
+    for (int64_t w = 1; w < W; ++w)
+        for (int64_t e = 0; e < N * d; ++e) {
+            dk[e] += ta[w].dk[e];
+            dv[e] += ta[w].dv[e];
+        }
+    free(ta); free(part);
 }
 
 int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
@@ -453,7 +568,8 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
     if (!(drop_p >= 0.0 && drop_p < 1.0)) return ORACLE_ERR_ARG;
     bwd_ctx_t c = {q, k, v, dout, H, N, d, scale, causal, kv_len, window, block_mask, block,
                    drop_p, seed, dq, dk, dv, ORACLE_OK};
-    run_pool(bwd_task, &c, (int64_t)B * H, nthreads);
+    outer_ctx_t oc = {&c, inner_threads((int64_t)B * H, nthreads)};
+    run_pool(bwd_task, &oc, (int64_t)B * H, nthreads);
     return c.err;
 }
 
