@@ -142,3 +142,41 @@ def attention_inputs(seed, B, H, N, d, with_dout=True):
     """bf16 bit patterns of Q, K, V (and dO) for one workload, each [B,H,N,d]."""
     names = ("Q", "K", "V", "dO") if with_dout else ("Q", "K", "V")
     return {nm: normal_bf16_bits(seed, STREAM[nm], (B, H, N, d)) for nm in names}
+
+
+def _round_to(x, fmt):
+    if fmt == "bf16":
+        return f32_to_bf16_bits(np.asarray(x, np.float64).astype(np.float32))
+    if fmt == "e4m3":
+        return f32_to_e4m3_bits(x)
+    raise ValueError("fmt must be 'bf16' or 'e4m3'")
+
+
+def shaped_key_inputs(seed, B, H, N, d, gain=None, levels=None, noise=1.0, v_shift=0.0,
+                      fmt="bf16", with_dout=True):
+    """Inputs whose attention scores rise along the key axis, so that a row's
+    running maximum grows by many units after the first key blocks.
+
+    The draws are those of `attention_inputs` (same seed and streams); only
+    their shape changes:
+      - `gain` (fp64 [N] or None): key row j is multiplied by gain[j];
+      - `levels` (fp64 [N] or None): column 0 of every query row is set to 1,
+        column 0 of key row j to levels[j], and the other key columns are
+        multiplied by `noise`; the score of any query with key j is then
+        levels[j] plus a term of spread `noise * sqrt(d - 1)` (before the
+        caller's scale);
+      - `v_shift`: added to every value of V (a nonzero mean makes any
+        weighted average of V rows differ from zero).
+    Values are rounded to bf16 (uint16 bits) or to e4m3 codes (uint8; fmt =
+    "e4m3": Q, K, V only)."""
+    names = ("Q", "K", "V", "dO") if (with_dout and fmt == "bf16") else ("Q", "K", "V")
+    shape = (B, H, N, d)
+    x = {nm: normal_f64(seed, STREAM[nm], B * H * N * d).reshape(shape) for nm in names}
+    if gain is not None:
+        x["K"] = x["K"] * np.asarray(gain, np.float64).reshape(1, 1, N, 1)
+    if levels is not None:
+        x["K"] = x["K"] * noise
+        x["K"][..., 0] = np.asarray(levels, np.float64).reshape(1, 1, N)
+        x["Q"][..., 0] = 1.0
+    x["V"] = x["V"] + v_shift
+    return {nm: _round_to(v, fmt) for nm, v in x.items()}
