@@ -109,7 +109,42 @@ def test_sweep_sampled(d, N, causal):
     B, Hh = 16384 // N, 2048 // d
     case = H.Case(1004, B, Hh, N, d)
     rows = np.unique(np.array([0, 1, N // 2, N - 129, N - 128, N - 1]))
-    check_sampled(case, causal, [(B - 1, Hh - 1)], rows, rows)
+    check_sampled(case, causal, [(0, 0), (B // 2, Hh // 2), (B - 1, Hh - 1)], rows, rows)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_whole_head(causal):
+    """Every element of O, L, dQ, dK and dV of one head of the benchmark
+    workload (B=1, H=16, N=16384, d=128, all 16 heads launched together, as
+    the benchmark times them) against the oracle run on that head's slice.
+    The oracle deals the head's row panels out to the host threads: about
+    0.5 TFLOP of fp64 work non-causal, some 15-40 s on 16 host cores."""
+    from exact_io_aware_40_gb300 import fa
+    case = H.Case(1003, 1, 16, 16384, 128)
+    q, k, v, do = (case.dev[n] for n in ("Q", "K", "V", "dO"))
+    o, L = fa.attention_fwd(q, k, v, causal=causal, scale=case.scale)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, L, causal=causal, scale=case.scale)
+    fa.fa_check_error()
+    h = 5
+    sl = {n: case.f64[n][:, h:h + 1] for n in ("Q", "K", "V", "dO")}
+    o_ref, L_ref = oracle.attn_fwd(sl["Q"], sl["K"], sl["V"], case.scale, causal)
+    g_ref = oracle.attn_bwd(sl["Q"], sl["K"], sl["V"], sl["dO"], case.scale, causal)
+    o_h, L_h = H.to_f64(o[:, h:h + 1]), H.to_f64(L[:, h:h + 1])
+    assert H.err_o(o_h, o_ref) <= H.TOL_O_ABS, ("O", H.err_o(o_h, o_ref))
+    assert H.err_l(L_h, L_ref) <= H.TOL_L_ABS, ("L", H.err_l(L_h, L_ref))
+    errs = [H.err_rel(H.to_f64(g[:, h:h + 1]), r) for g, r in zip((dq, dk, dv), g_ref)]
+    H.report("whole_head", case, causal, err_O=H.err_o(o_h, o_ref), err_L=H.err_l(L_h, L_ref),
+             err_dQ=errs[0], err_dK=errs[1], err_dV=errs[2])
+    for name, e in zip(("dQ", "dK", "dV"), errs):
+        assert e <= H.TOL_GRAD_REL, (name, e)
+
+
+@pytest.mark.parametrize("factor", [0.5, 2.0])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_other_scales(factor, d, causal):
+    # scales other than 1/sqrt(d) on the usual iid inputs
+    check_full(H.Case(4100 + d, 2, 2, 700, d, scale=factor / np.sqrt(d)), causal)
 
 
 def test_deterministic():

@@ -115,6 +115,14 @@ def test_sweep_sampled_rows(d, N, causal):
     check_rows(case, causal, [(0, 0), (B - 1, Hh - 1)], rows)
 
 
+@pytest.mark.parametrize("factor", [0.5, 2.0])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_other_scales(factor, d, causal):
+    # scales other than 1/sqrt(d) on the usual iid inputs
+    check_full(H.Case(2100 + d, 2, 2, 700, d, scale=factor / np.sqrt(d)), causal)
+
+
 def test_deterministic():
     case = H.Case(1005, 2, 4, 700, 128)
     o1, L1 = run_fwd(case, True)
