@@ -15,6 +15,37 @@
 
 namespace fa {
 
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static std::atomic<void*> fn_cur{nullptr}, fn_id{nullptr};
+  void* fc = fn_cur.load(std::memory_order_acquire);
+  void* fi = fn_id.load(std::memory_order_acquire);
+  if (fc == nullptr || fi == nullptr) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fc, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || fc == nullptr)
+      return false;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fi, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || fi == nullptr)
+      return false;
+    fn_cur.store(fc, std::memory_order_release);
+    fn_id.store(fi, std::memory_order_release);
+  }
+  CUcontext ctx = nullptr;
+  if (reinterpret_cast<GetCurrentFn>(fc)(&ctx) != CUDA_SUCCESS) return false;
+  if (ctx == nullptr) {
+    // No context yet on this thread: cudaSetDevice makes the device's primary
+    // context current (initialising it if needed).
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+    if (reinterpret_cast<GetCurrentFn>(fc)(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  }
+  return reinterpret_cast<GetIdFn>(fi)(ctx, id) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static std::atomic<int> cached[64] = {};
   int dev = 0;
@@ -47,6 +78,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
+unsigned long long g_err_ctx[kMaxDevices] = {};
 EncodeTiledFn g_encode = nullptr;
 
 fa_status current_device(int* dev) {
@@ -55,13 +87,17 @@ fa_status current_device(int* dev) {
   return FA_OK;
 }
 
-// Device address of this device's error word (cached per device).
+// Device address of this device's error word, cached per device and looked
+// up again when the device's context has changed (after a device reset).
 fa_status error_word(int dev, int** out) {
+  unsigned long long ctx = 0;
+  if (!fa::current_context_id(&ctx)) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_err_ptr[dev] == nullptr) {
+  if (g_err_ptr[dev] == nullptr || g_err_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
     g_err_ptr[dev] = static_cast<int*>(p);
+    g_err_ctx[dev] = ctx;
   }
   *out = g_err_ptr[dev];
   return FA_OK;

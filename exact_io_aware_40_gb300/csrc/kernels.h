@@ -28,6 +28,12 @@ struct FwdArgs {
 // Multiprocessors of the current device (cached per device; 0 on error).
 int sm_count();
 
+// Unique id of the calling thread's current CUDA context (the driver never
+// reuses one within a process, so a device reset shows up as a new id).
+// Device addresses of this library's __device__ variables are cached under
+// it.  Returns false on a driver error.
+bool current_context_id(unsigned long long* id);
+
 // Group width for cta_tile.  Only a causal mask without a window gives the
 // CTAs of a launch very different amounts of work (the longest tile has
 // n_tiles times the shortest's; a window makes them about equal); then one

@@ -232,16 +232,20 @@ fa_status fa_bwd_dq(const void* Q, const void* K, const void* V, const void* dO,
  * device memory -- code running under a host framework that owns every device
  * byte through its own pool, and latency-critical paths on which cudaMalloc or
  * cudaFree could synchronise the device.  It computes exactly what fa_bwd
- * computes (same kernels, same arguments minus the workspace) and allocates
- * nothing: its workspace is a file-scope device array of
- * FA_BWD_NOALLOC_SCRATCH_BYTES bytes inside this library.
+ * computes (same kernels, same arguments minus the workspace, every head
+ * dimension fa_bwd takes: 64, 128, 256) and allocates nothing: its workspace
+ * is a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES bytes inside
+ * this library.
  *   - Size limit: returns FA_ERR_UNSUPPORTED, and enqueues nothing, when
  *     fa_bwd_workspace_bytes(B, H, N, d) exceeds FA_BWD_NOALLOC_SCRATCH_BYTES,
  *     i.e. when B * H * N exceeds 4,194,304 rows (B=1, H=16, N=16384 fits;
- *     B=8, H=64, N=8200 does not).
+ *     B=8, H=64, N=8200 does not), and for a head dimension other than 64,
+ *     128 or 256.
  *   - First call on a device: looks up the array's device address there
  *     (cudaGetSymbolAddress, which may load the library's device code on that
- *     device).  Make that first call before any stream capture.
+ *     device).  Make that first call before any stream capture.  The address
+ *     is cached per device and looked up again when the device's context has
+ *     changed (after cudaDeviceReset, for example).
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents; each call overwrites what it reads before reading
  *     it.  Calls whose work overlaps on the GPU (different streams without

@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 
 import helpers as H
+from oracle import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +51,7 @@ def test_noalloc_matches_fa_bwd_on_calls_in_a_row(lib):
     cases = [
         (H.Case(7001, 2, 4, 1000, 128), False),
         (H.Case(7002, 4, 8, 777, 64, kv_range=(300, 777)), True),
+        (H.Case(7003, 1, 4, 600, 256), True),
     ]
     # the first shape again after the second: stale scratch must not leak in
     for case, causal in cases + cases[:1]:
@@ -77,6 +79,34 @@ def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
     L = torch.zeros(B, Hh, N, dtype=torch.float32, device="cuda")
     st = lib.fa_bwd_noalloc(_p(x), _p(x), _p(x), _p(x), _p(x), _p(L), _p(x), _p(x), _p(x),
                             B, Hh, N, d, ctypes.c_float(0.125), 0, _p(None),
+                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == fa.FA_ERR_UNSUPPORTED
+    fa.fa_check_error()
+
+
+def test_noalloc_matches_the_oracle(lib):
+    # d = 256 with key padding, compared with the fp64 oracle directly
+    from exact_io_aware_40_gb300 import fa
+    case = H.Case(7004, 2, 2, 333, 256)
+    case.set_kv_len([333, 150])
+    q, k, v = (case.dev[n] for n in ("Q", "K", "V"))
+    o, L = fa.attention_fwd(q, k, v, causal=True, scale=case.scale, kv_len=case.kv_len_dev)
+    got = noalloc_bwd(lib, case, o, L, True)
+    fa.fa_check_error()
+    ref = oracle.attn_bwd(case.f64["Q"], case.f64["K"], case.f64["V"], case.f64["dO"],
+                          case.scale, True, kv_len=case.kv_len)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        e = H.err_rel(H.to_f64(g), r)
+        assert e <= H.TOL_GRAD_REL, (name, e)
+
+
+def test_noalloc_refuses_an_unsupported_head_dim(lib):
+    import torch
+    from exact_io_aware_40_gb300 import fa
+    x = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device="cuda")
+    L = torch.zeros(1, 1, 64, dtype=torch.float32, device="cuda")
+    st = lib.fa_bwd_noalloc(_p(x), _p(x), _p(x), _p(x), _p(x), _p(L), _p(x), _p(x), _p(x),
+                            1, 1, 64, 96, ctypes.c_float(0.1), 0, _p(None),
                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == fa.FA_ERR_UNSUPPORTED
     fa.fa_check_error()
