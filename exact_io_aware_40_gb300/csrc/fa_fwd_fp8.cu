@@ -8,10 +8,17 @@
 // with one fp32 dequantisation factor per tensor (value = factor * code), so
 // S = scale * (dq Q8)(dk K8)^T and O = softmax(S) (dv V8); the products run on
 // the tensor cores in kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate), at twice
-// the bf16 rate.  P enters the PV product rounded to e4m3 (P <= 2^8 here, well
-// inside its range); O is divided by the row sum of those rounded weights, so
-// the weights applied to V sum to one exactly, and L uses the sum of the
-// unrounded P.  O is written in bf16.
+// the bf16 rate.  P enters the PV product rounded to e4m3; O is divided by the
+// row sum of those rounded weights, so the weights applied to V sum to one
+// exactly, and L uses the sum of the unrounded P.  O is written in bf16.
+// e4m3 holds normal values from 2^-6 to 448 only: weights taken relative to
+// the row maximum alone would fall into its subnormal range, or to zero, once
+// they are 2^-7 of the maximum or less, and hundreds of such keys can carry
+// much of a row's weight after its maximum has jumped.  So P is computed as
+// 2^(s - m + 6) (s, m in log2 units): weights down to 2^-12 of the maximum
+// stay normal, and with the rescale threshold at 2 the largest weight is at
+// most 2^8 = 256 < 448.  The common factor 2^6 cancels in O and is taken out
+// of L.
 //
 // GB300 mapping: one 128-row query block per CTA, 128-key blocks.  With d =
 // 128 one row of Q, K or V^T is 128 bytes, one 128-byte swizzle atom, and
@@ -36,7 +43,8 @@ constexpr int kBR = 128;      // query rows per CTA (MMA M)
 constexpr int kBC = 128;      // keys per block (MMA N of S, K of PV)
 constexpr int kD = 128;       // head dimension
 constexpr int kThreads = 192;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 8
+constexpr float kRescaleThreshold = 2.0f;  // log2 units: rescale O only if m grows by > 2
+constexpr float kPOffset = 6.0f;           // P = 2^(s - m + kPOffset), at most 2^8
 constexpr float kLn2 = 0.693147180559945309f;
 
 constexpr int kTile8 = 128 * 128;  // 128 rows x 128 one-byte elements
@@ -261,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool grow_max = m_cand > m_run + kRescaleThreshold;
       const float m_new = grow_max ? m_cand : m_run;
       const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // P = 2^(s * scale * log2e - m), rounded to e4m3 into this row of P's
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new - kPOffset;
+      // P = 2^(s * scale * log2e - m + 6), rounded to e4m3 into this row of P's
       // shared-memory tile (the 128-byte swizzle TMA and the tensor core use:
       // 16-byte chunk t of row r at chunk t ^ (r % 8)).
       const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue
       const float inv_l = lh_run > 0.f ? a.out_scale / lh_run : 0.f;
       if (grow < a.N) {
-        const float Lv = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        const float Lv = l_run > 0.f ? (m_run - kPOffset + log2f(l_run)) * kLn2 : -INFINITY;
         a.L[static_cast<long long>(bh) * a.N + grow] = Lv;
       }
       // O * dv / lh -> bf16 -> staging tile (128-byte swizzle, two 64-column
