@@ -154,9 +154,10 @@ def rescaled_rows(q, k, scale, vis, rows, margin=0.25):
     return int((grow > 8.0 + margin).sum())
 
 
-def o_bound_dropout(o_ref, a_ref):
-    """Per-element O tolerance under dropout: the two bf16 roundings (the dropped
-    weights fed to the product and O itself), each at most 2^-9 relative, with
-    a factor two of margin, or 1e-2 where larger; a_ref = sum_j Pd_ij |v_jc|
-    (the oracle run on |V|)."""
+def o_bound_bf16(o_ref, a_ref):
+    """Per-element O tolerance where |O| can exceed 4 (dropout, or inputs whose
+    weights concentrate on few keys): the two bf16 roundings (the weights fed
+    to the product and O itself), each at most 2^-9 relative, with a factor two
+    of margin, or 1e-2 where larger; a_ref = sum_j w_ij |v_jc| with the weights
+    w the product applies (the oracle run on |V|)."""
     return np.maximum(TOL_O_ABS, 2.0 ** -8 * (np.abs(o_ref) + a_ref))

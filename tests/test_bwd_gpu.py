@@ -108,7 +108,10 @@ def test_long_sequence_sampled(causal):
 def test_sweep_sampled(d, N, causal):
     B, Hh = 16384 // N, 2048 // d
     case = H.Case(1004, B, Hh, N, d)
-    rows = np.unique(np.array([0, 1, N // 2, N - 129, N - 128, N - 1]))
+    # The tolerance is relative to the tensor's max norm; the sampled rows
+    # include the early ones, where causal rows (few keys) have the largest
+    # gradients, so the max over the sample stands for the tensor's.
+    rows = np.unique(np.array([0, 1, 2, 3, 64, 127, 128, 129, N // 2, N - 129, N - 128, N - 1]))
     check_sampled(case, causal, [(0, 0), (B // 2, Hh // 2), (B - 1, Hh - 1)], rows, rows)
 
 

@@ -17,7 +17,16 @@ tenfold.
 
 Every plain forward instantiation (d = 64, 128, 256; causal or not), the
 window / block-mask and dropout instantiations, the e4m3 forward, scales
-other than 1/sqrt(d), and sampled rows at 16K tokens are covered."""
+other than 1/sqrt(d), and sampled rows at 16K tokens are covered.
+
+O tolerance.  On these inputs a row's weights can concentrate on one key,
+so |O| reaches 4 and more, where the spacing of bf16 is 2^-5 and even the
+correctly rounded exact value can miss a flat 1e-2.  O is therefore checked
+against the bound the bf16 arithmetic allows (the same as under dropout):
+two bf16 roundings, of the weights fed to the product and of O, each at
+most 2^-9 relative, with a factor two of margin --
+|dO_ic| <= max(1e-2, 2^-8 (|O_ic| + sum_j p_ij |v_jc|)), the sum taken by the
+oracle on |V|.  L and the gradients keep their tolerances."""
 import numpy as np
 import pytest
 
@@ -78,12 +87,9 @@ def check_full(case, causal, window=-1, bm=None, p=0.0, seed=0):
     kw = dict(kv_len=case.kv_len, window=window, block_mask=bm, block=128, dropout_p=pp,
               seed=seed)
     o_ref, L_ref = oracle.attn_fwd(*args, case.scale, causal, **kw)
-    if p > 0.0:
-        a_ref, _ = oracle.attn_fwd(args[0], args[1], np.abs(args[2]), case.scale, causal, **kw)
-        excess = np.abs(o - o_ref) - H.o_bound_dropout(o_ref, a_ref)
-        assert excess.max() <= 0.0, ("O", float(np.abs(o - o_ref).max()))
-    else:
-        assert H.err_o(o, o_ref) <= H.TOL_O_ABS, ("O", H.err_o(o, o_ref))
+    a_ref, _ = oracle.attn_fwd(args[0], args[1], np.abs(args[2]), case.scale, causal, **kw)
+    excess = np.abs(o - o_ref) - H.o_bound_bf16(o_ref, a_ref)
+    assert excess.max() <= 0.0, ("O", float(np.abs(o - o_ref).max()), float(excess.max()))
     assert H.err_l(L, L_ref) <= H.TOL_L_ABS, ("L", H.err_l(L, L_ref))
     g_ref = oracle.attn_bwd(*args, case.f64["dO"], case.scale, causal, **kw)
     errs = [H.err_rel(g, r) for g, r in zip((dq, dk, dv), g_ref)]
@@ -173,7 +179,8 @@ def test_rescale_long_sequence_sampled(kind, causal):
     for h in range(2):
         qh, kh, vh, doh = (case.f64[n][0, h] for n in ("Q", "K", "V", "dO"))
         o_ref, L_ref = oracle.fwd_rows(qh, kh, vh, case.scale, causal, N, rows)
-        assert H.err_o(o[0, h, rows], o_ref) <= H.TOL_O_ABS
+        a_ref, _ = oracle.fwd_rows(qh, kh, np.abs(vh), case.scale, causal, N, rows)
+        assert (np.abs(o[0, h, rows] - o_ref) - H.o_bound_bf16(o_ref, a_ref)).max() <= 0.0
         assert H.err_l(L[0, h, rows], L_ref) <= H.TOL_L_ABS
         dq_ref = oracle.bwd_dq_rows(qh, kh, vh, doh, case.scale, causal, N, rows)
         dk_ref, dv_ref = oracle.bwd_dkdv_cols(qh, kh, vh, doh, case.scale, causal, N, rows)
