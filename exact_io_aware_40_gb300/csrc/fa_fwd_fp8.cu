@@ -8,9 +8,13 @@
 // with one fp32 dequantisation factor per tensor (value = factor * code), so
 // S = scale * (dq Q8)(dk K8)^T and O = softmax(S) (dv V8); the products run on
 // the tensor cores in kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate), at twice
-// the bf16 rate.  P enters the PV product rounded to e4m3; O is divided by the
-// row sum of those rounded weights, so the weights applied to V sum to one
-// exactly, and L uses the sum of the unrounded P.  O is written in bf16.
+// the bf16 rate.  P enters the PV product rounded to e4m3, and O is divided
+// by the row sum of the unrounded P (the sum L uses as well): the weights
+// applied to V then differ from P by the e4m3 rounding alone, at most 2^-4 of
+// each, so |O - O_exact| <= 2^-4 sum_j p_j |v_j|.  (Summing the rounded
+// weights instead would take three more conversions per pair of elements, and
+// the softmax, not the tensor pipe, bounds this kernel.)  O is written in
+// bf16.
 // e4m3 holds normal values from 2^-6 to 448 only: weights taken relative to
 // the row maximum alone would fall into its subnormal range, or to zero, once
 // they are 2^-7 of the maximum or less, and hundreds of such keys can carry
@@ -231,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float m_run = -INFINITY;                // running max, log2 units (scaled)
     float l_run = 0.f;                      // row sum of P
-    float lh_run = 0.f;                     // row sum of P rounded to e4m3
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int bb = j & 1;
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16-byte chunk t of row r at chunk t ^ (r % 8)).
       const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t nm2 = f2_pack(-m_use, -m_use);
-      uint64_t se[2] = {0ull, 0ull}, sh[2] = {0ull, 0ull};
+      uint64_t se[2] = {0ull, 0ull};
       uint8_t* prow = smem + kOffP + bb * kTile8 + row * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -292,10 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[e >> 1] |= q8 << 16;
           else
             w[e >> 1] = q8;
-          float r0, r1;
-          unpack_e4m3(q8, r0, r1);
           se[e & 1] = f2_add(se[e & 1], f2_pack(p0, p1));
-          sh[e & 1] = f2_add(sh[e & 1], f2_pack(r0, r1));
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -310,8 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float u0, u1;
       f2_unpack(f2_add(se[0], se[1]), u0, u1);
       l_run = l_run * alpha + (u0 + u1);
-      f2_unpack(f2_add(sh[0], sh[1]), u0, u1);
-      lh_run = lh_run * alpha + (u0 + u1);
       m_run = m_new;
       if (j > 0 && __any_sync(0xffffffffu, grow_max)) {
         // O holds P_0..P_{j-1} V; rescale it once PV_{j-1} has landed (only
@@ -343,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = bar_and_128(1, ok && *abort_flag == 0);
     if (ok) {
       // ---------------------------------------------------------- epilogue
-      const float inv_l = lh_run > 0.f ? a.out_scale / lh_run : 0.f;
+      const float inv_l = l_run > 0.f ? a.out_scale / l_run : 0.f;
       if (grow < a.N) {
         const float Lv = l_run > 0.f ? (m_run - kPOffset + log2f(l_run)) * kLn2 : -INFINITY;
         a.L[static_cast<long long>(bh) * a.N + grow] = Lv;

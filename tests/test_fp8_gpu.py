@@ -3,11 +3,12 @@ the dequantised inputs (factor x code, exact in fp64).
 
 The products are exact up to fp32 accumulation, so L keeps its 1e-3
 tolerance.  P enters the PV product rounded to e4m3 (3 mantissa bits: each
-weight within 2^-4 relative), and O is divided by the sum of those rounded
-weights, so O - O_ref = sum_j (w_j - p_j)(v_j - O_ref) with |w_j - p_j| <=
-2^-4 p_j to first order: |dO_ic| <= 2^-4 sum_j p_ij |v_jc - O_ic| <= 2^-4 (A_ic
-+ |O_ic|), A = sum_j p_ij |v_jc| (the oracle on |V|), plus the bf16 rounding of
-O (2^-8 |O| with margin).  The check is that bound, or 1e-2 where larger."""
+weight w_j within 2^-4 of p_j relative), and O is divided by the sum of the
+unrounded weights, so O - O_ref = sum_j (w_j - p_j) v_jc / sum_j p_j and
+|dO_ic| <= 2^-4 A_ic, A = sum_j p_ij |v_jc| (the oracle on |V|), plus the bf16
+rounding of O (2^-8 |O| with margin).  The check allows 2^-4 (A_ic + |O_ic|) +
+2^-8 |O_ic|, or 1e-2 where larger: the bound of dividing by the sum of the
+rounded weights instead, which contains this one."""
 import numpy as np
 import pytest
 
