@@ -32,13 +32,21 @@ def run_fwd(case, causal):
     return H.to_f64(o), H.to_f64(L)
 
 
-def check_full(case, causal):
+def check_full(case, causal, derived_o_bound=False):
+    """derived_o_bound: check O against the bound of the bf16 arithmetic
+    (helpers.o_bound_bf16) instead of a flat 1e-2 -- for inputs outside the
+    five workloads, where weights concentrate and |O| can exceed 2."""
     o, L = run_fwd(case, causal)
     o_ref, L_ref = oracle.attn_fwd(case.f64["Q"], case.f64["K"], case.f64["V"], case.scale,
                                    causal, kv_len=case.kv_len)
     eo, el = H.err_o(o, o_ref), H.err_l(L, L_ref)
     H.report("fwd", case, causal, err_O=eo, err_L=el)
-    assert eo <= H.TOL_O_ABS, ("O", eo)
+    if derived_o_bound:
+        a_ref, _ = oracle.attn_fwd(case.f64["Q"], case.f64["K"], np.abs(case.f64["V"]),
+                                   case.scale, causal, kv_len=case.kv_len)
+        assert (np.abs(o - o_ref) - H.o_bound_bf16(o_ref, a_ref)).max() <= 0.0, ("O", eo)
+    else:
+        assert eo <= H.TOL_O_ABS, ("O", eo)
     assert el <= H.TOL_L_ABS, ("L", el)
     return eo, el
 
@@ -119,8 +127,11 @@ def test_sweep_sampled_rows(d, N, causal):
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_other_scales(factor, d, causal):
-    # scales other than 1/sqrt(d) on the usual iid inputs
-    check_full(H.Case(2100 + d, 2, 2, 700, d, scale=factor / np.sqrt(d)), causal)
+    # scales other than 1/sqrt(d) on the usual iid inputs; at twice the usual
+    # scale the weights concentrate and |O| exceeds 2, where bf16 rounding
+    # alone approaches 1e-2: O is checked against the bf16-derived bound
+    check_full(H.Case(2100 + d, 2, 2, 700, d, scale=factor / np.sqrt(d)), causal,
+               derived_o_bound=True)
 
 
 def test_deterministic():
