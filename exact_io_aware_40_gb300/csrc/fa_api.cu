@@ -217,11 +217,10 @@ const char* fa_status_string(fa_status s) {
 
 namespace {
 
-// window < -1 is invalid; the window and block-mask terms run on the d = 64
-// and d = 128 kernels.
-fa_status check_mask(int d, int window, const uint8_t* block_mask) {
+// window < -1 is invalid; the window and block-mask terms run at every head
+// dimension.
+fa_status check_mask(int window) {
   if (window < -1) return FA_ERR_INVALID_ARG;
-  if ((window >= 0 || block_mask != nullptr) && d == 256) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -231,7 +230,7 @@ struct Drop {
   uint32_t thr = 0, seed_lo = 0, seed_hi = 0;
   float scale = 1.f;
 };
-fa_status make_drop(int d, float p, uint64_t seed, Drop* out) {
+fa_status make_drop(float p, uint64_t seed, Drop* out) {
   if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;
   Drop z;
   const double t = std::floor(static_cast<double>(p) * 65536.0);
@@ -239,7 +238,6 @@ fa_status make_drop(int d, float p, uint64_t seed, Drop* out) {
   z.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
   z.seed_hi = static_cast<uint32_t>(seed >> 32);
   z.scale = static_cast<float>(65536.0 / (65536.0 - static_cast<double>(z.thr)));
-  if (z.thr != 0 && d == 256) return FA_ERR_UNSUPPORTED;
   *out = z;
   return FA_OK;
 }
@@ -251,9 +249,9 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
-  if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
+  if ((st = check_mask(window)) != FA_OK) return st;
   Drop drop;
-  if ((st = make_drop(d, dropout_p, seed, &drop)) != FA_OK) return st;
+  if ((st = make_drop(dropout_p, seed, &drop)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4) ||
       (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
@@ -416,9 +414,9 @@ static fa_status bwd_args(const void* Q, const void* K, const void* V, const voi
   if (!Q || !K || !V || !dO || !L) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
-  if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
+  if ((st = check_mask(window)) != FA_OK) return st;
   Drop drop;
-  if ((st = make_drop(d, dropout_p, seed, &drop)) != FA_OK) return st;
+  if ((st = make_drop(dropout_p, seed, &drop)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) ||
       !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))
     return FA_ERR_INVALID_ARG;
@@ -507,9 +505,9 @@ static fa_status bwd_impl(const void* Q, const void* K, const void* V, const voi
     return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
-  if ((st = check_mask(d, window, block_mask)) != FA_OK) return st;
+  if ((st = check_mask(window)) != FA_OK) return st;
   Drop drop;
-  if ((st = make_drop(d, dropout_p, seed, &drop)) != FA_OK) return st;
+  if ((st = make_drop(dropout_p, seed, &drop)) != FA_OK) return st;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
       !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
       !aligned(L, 4) || (kv_len && !aligned(kv_len, 4)))

@@ -28,6 +28,10 @@
 // instead of 5); in exchange dQ needs no fp32 accumulator, no reductions, and
 // is deterministic.
 #include "kernels.h"
+#include <type_traits>
+
+#include "masks.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -61,6 +65,46 @@ __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t atom) {
 // (two 8-row groups, SBO 1024 B); 64-column atoms are `atom` bytes apart (LBO).
 __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t atom) {
   return sdesc_sw128(base + k * 2048, atom, 1024);
+}
+
+// The steps of S rows (or keys) a CTA visits: the 128-blocks of a range from
+// the mask terms, thinned by a block-mask row or column (`m`, consecutive
+// blocks `stride` bytes apart; nullptr keeps all), each cut into steps of S,
+// and those of the block holding `limit` only up to it.  Every role walks the
+// same steps with its own cursor.
+template <int S>
+struct StepWalk {
+  const uint8_t* m;
+  int stride, hi, limit, blk, sub;
+  __device__ __forceinline__ void init(const uint8_t* m_, int stride_, int lo, int hi_,
+                                       int limit_) {
+    m = m_;
+    stride = stride_;
+    hi = hi_;
+    limit = limit_;
+    sub = 0;
+    blk = next_block(m, stride, lo, hi);
+  }
+  __device__ __forceinline__ int pos() const { return blk * kMaskBlock + sub * S; }
+  __device__ __forceinline__ void next() {
+    ++sub;
+    if (sub * S == kMaskBlock || pos() >= limit) {
+      sub = 0;
+      blk = next_block(m, stride, blk + 1, hi);
+    }
+  }
+};
+// Number of steps of such a walk; called by a whole warp.
+template <int S>
+__device__ __forceinline__ int count_steps(const uint8_t* m, int stride, int lo, int hi,
+                                           int limit) {
+  int n = count_blocks(m, stride, lo, hi) * (kMaskBlock / S);
+  const int lb = (limit - 1) / kMaskBlock;  // the block holding the last position
+  if (limit > 0 && lb >= lo && lb < hi && block_on(m, stride, lb)) {
+    const int in_last = (limit - lb * kMaskBlock + S - 1) / S;
+    n -= kMaskBlock / S - in_last;
+  }
+  return n;
 }
 
 // ===========================================================================
@@ -98,7 +142,9 @@ struct KvCfg {
   static_assert(4 * QS <= 256 && 256 + 2 * DH <= 512, "TMEM budget");
 };
 
-template <int HD, int DH, int QS>
+// DROP: dropout on P; MASKX: a sliding window or a block mask (separate
+// instantiations, as in the other kernels).
+template <int HD, int DH, int QS, bool DROP, bool MASKX>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -138,8 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hatom = half * (DH / 64);  // first 64-column atom of this CTA's half
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const int i_start = a.causal ? k0 / QS : 0;
-  const int n_iter = (k0 >= kv_limit) ? 0 : a.n_qtiles - i_start;
+  // Query steps of QS rows: the visible 128-row query blocks (a range from the
+  // key padding, causal and window terms, thinned by column kt of the block
+  // mask), each cut into steps, the last one up to row N.
+  const int window = MASKX ? a.window : -1;
+  int ilo, ihi;
+  query_block_range(kt, a.nb, kv_limit, a.causal, window, &ilo, &ihi);
+  const uint8_t* bmc = (MASKX && a.bmask) ? a.bmask + kt : nullptr;  // column kt, stride nb
+  const int n_iter = count_steps<QS>(bmc, a.nb, ilo, ihi, a.N);
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
@@ -188,9 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int last[C::kSt];
       for (int t = 0; t < C::kSt; ++t) last[t] = -1;
-      for (int it = 0; it < n_iter; ++it) {
+      StepWalk<QS> walk;
+      walk.init(bmc, a.nb, ilo, ihi, a.N);
+      for (int it = 0; it < n_iter; ++it, walk.next()) {
         const int st = it % C::kSt;
-        const int q0 = (i_start + it) * QS;
+        const int q0 = walk.pos();
         if (it >= C::kSt &&
             !__all_sync(0xffffffffu, mbar_wait(bar_qdo_empty(st), ((it / C::kSt) & 1) ^ 1, ab)))
           break;
@@ -290,18 +344,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t cs = 2u * QS * x, cdp = 2u * QS * x + QS;
     const bool key_ok = key < kv_limit;
     bool ok = true;
-    for (int it = x, n = 0; it < n_iter; it += 2, ++n) {
+    StepWalk<QS> walk;  // this warpgroup's steps: x, x + 2, ...
+    walk.init(bmc, a.nb, ilo, ihi, a.N);
+    if (x) walk.next();
+    for (int it = x, n = 0; it < n_iter; it += 2, ++n, walk.next(), walk.next()) {
       const int st = it % C::kSt;
-      const int q0 = (i_start + it) * QS;
+      const int q0 = walk.pos();
       const float* L2 = sLD + st * 2 * QS;
       const float* Dv = L2 + QS;
+      // Dropout keep bits of this thread's key for the step's QS queries (the
+      // warp draws them together).
+      uint32_t km = 0;
+      if constexpr (DROP) {
+        static_assert(QS == 32, "keep bits for 32-query steps");
+        km = keep32_transposed(static_cast<uint32_t>(k0 + quarter * 32), static_cast<uint32_t>(q0),
+                               static_cast<uint32_t>(bh % a.H), static_cast<uint32_t>(b), a.seed_lo,
+                               a.seed_hi, a.drop_thr);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar_ld_full(st), (it / C::kSt) & 1, ab) &&
                                        mbar_wait(bar_s(x), n & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool need_mask = !key_ok || (q0 + QS > a.N) || (a.causal && q0 < k0 + kKeys - 1);
+      const bool band = (a.causal != 0) | (window >= 0);
+      const bool need_mask = !key_ok || (q0 + QS > a.N) || (band && q0 < k0 + kKeys - 1) ||
+                             (window >= 0 && k0 < q0 + QS - 1 - window);
       float p[QS];
 #pragma unroll
       for (int c = 0; c < QS / 32; ++c) {
@@ -320,12 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int qg = q0 + 32 * c + e;
-            const bool keep = key_ok & (qg < a.N) & !((a.causal != 0) & (key > qg));
+            const bool keep = (qg < a.N) & visible(qg, key, kv_limit, a.causal, window);
             p[32 * c + e] = keep ? p[32 * c + e] : 0.f;
           }
         }
+        // dV takes the dropped weights P Z / q; p itself stays for dS^T.
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) {
+          const int qa = 32 * c + 2 * e;
+          if constexpr (DROP)
+            w[e] = pack_bf16((km >> qa) & 1u ? p[qa] * a.drop_scale : 0.f,
+                             (km >> (qa + 1)) & 1u ? p[qa + 1] * a.drop_scale : 0.f);
+          else
+            w[e] = pack_bf16(p[qa], p[qa + 1]);
+        }
         tmem_st16(tl + cs + 16 * c, w);  // P^T: first 32 columns of the S^T buffer
       }
       tmem_wait_st();
@@ -347,8 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int qa = 32 * c + 2 * e;
-          const float d0 = p[qa] * (__uint_as_float(dr[2 * e]) - Dv[qa]);
-          const float d1 = p[qa + 1] * (__uint_as_float(dr[2 * e + 1]) - Dv[qa + 1]);
+          // dS^T = P^T o (dP^T - D); with dropout dP^T = (V dO^T) Z / q.
+          float g0 = __uint_as_float(dr[2 * e]), g1 = __uint_as_float(dr[2 * e + 1]);
+          if constexpr (DROP) {
+            g0 = (km >> qa) & 1u ? g0 * a.drop_scale : 0.f;
+            g1 = (km >> (qa + 1)) & 1u ? g1 * a.drop_scale : 0.f;
+          }
+          const float d0 = p[qa] * (g0 - Dv[qa]);
+          const float d1 = p[qa + 1] * (g1 - Dv[qa + 1]);
           w[e] = pack_bf16(d0, d1);
         }
         // dS^T columns [16c, 16c+16) overwrite dP^T columns this thread has read.
@@ -434,7 +516,7 @@ struct QCfg {
   static_assert(4 * KS <= 256 && 256 + QT * HD <= 512, "TMEM budget");
 };
 
-template <int HD, int QT, int KS>
+template <int HD, int QT, int KS, bool DROP, bool MASKX>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -469,13 +551,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / a.H;
   int kv_limit = a.N;
   if (a.kv_len != nullptr) kv_limit = min(max(a.kv_len[b], 0), a.N);
-  const int kv_steps = (kv_limit + KS - 1) / KS;
-  const bool hasB = QT == 2 && qtA + 1 < a.n_qtiles;
-  // key steps each query block needs: keys <= last row of the block (causal)
-  const int TA = a.causal ? min(kv_steps, (qtA * kQRows + kQRows - 1) / KS + 1) : kv_steps;
-  const int TB =
-      hasB ? (a.causal ? min(kv_steps, ((qtA + 1) * kQRows + kQRows - 1) / KS + 1) : kv_steps) : 0;
-  const int T = max(TA, TB);
+  static_assert(QT == 1, "one query block per CTA");
+  constexpr bool hasB = false;
+  // Key steps of KS keys: the visible 128-key blocks (a range from the key
+  // padding, causal and window terms, thinned by row qtA of the block mask),
+  // each cut into steps, the last one up to kv_len.
+  const int window = MASKX ? a.window : -1;
+  int jlo, jhi;
+  key_block_range(qtA, kv_limit, a.causal, window, &jlo, &jhi);
+  const uint8_t* bmr = (MASKX && a.bmask) ? a.bmask + static_cast<long long>(qtA) * a.nb : nullptr;
+  const int TA = count_steps<KS>(bmr, 1, jlo, jhi, kv_limit);
+  constexpr int TB = 0;
+  const int T = TA;
 
   if (tid == 0) {
     mbar_init(bar_qfull(0), 1);
@@ -525,14 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int last[C::kSt];
       for (int s = 0; s < C::kSt; ++s) last[s] = -1;
-      for (int j = 0; j < T; ++j) {
+      StepWalk<KS> walk;
+      walk.init(bmr, 1, jlo, jhi, kv_limit);
+      for (int j = 0; j < T; ++j, walk.next()) {
         const int st = j % C::kSt;
         if (j >= C::kSt && !mbar_wait(bar_kvempty(st), ((j / C::kSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_kvfull(st), 2 * C::kKTile);
         for (int c = 0; c < C::kAtoms; ++c) {
-          tma_load_3d(sK + st * C::kKTile + c * C::kKAtom, &tmK, c * 64, j * KS, bh,
+          tma_load_3d(sK + st * C::kKTile + c * C::kKAtom, &tmK, c * 64, walk.pos(), bh,
                       bar_kvfull(st), pol_kv);
-          tma_load_3d(sV + st * C::kKTile + c * C::kKAtom, &tmV, c * 64, j * KS, bh,
+          tma_load_3d(sV + st * C::kKTile + c * C::kKAtom, &tmV, c * 64, walk.pos(), bh,
                       bar_kvfull(st), pol_kv);
         }
         last[st] = j;
@@ -610,14 +699,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float L2 = grow < a.N ? a.L[ridx] * kLog2e : 0.f;
     const float Dr = grow < a.N ? a.D[ridx] : 0.f;
     bool ok = true;
-    for (int j = 0; j < Tn; ++j) {
+    StepWalk<KS> walk;
+    walk.init(bmr, 1, jlo, jhi, kv_limit);
+    for (int j = 0; j < Tn; ++j, walk.next()) {
+      const int key0 = walk.pos();
+      // Dropout keep bits of this row's KS keys, drawn before S arrives.
+      uint32_t km = 0;
+      if constexpr (DROP) {
+        static_assert(KS == 32, "keep bits for 32-key steps");
+        km = keep32(static_cast<uint32_t>(key0), static_cast<uint32_t>(grow),
+                    static_cast<uint32_t>(bh % a.H), static_cast<uint32_t>(b), a.seed_lo,
+                    a.seed_hi, a.drop_thr);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s(x), j & 1, ab))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int key0 = j * KS;
-      const bool need_mask = (key0 + KS > kv_limit) || (a.causal && key0 + KS - 1 > q0);
+      const bool band = (a.causal != 0) | (window >= 0);
+      const bool need_mask = (key0 + KS > kv_limit) || (band && key0 + KS - 1 > q0) ||
+                             (window >= 0 && key0 < q0 + kQRows - 1 - window);
       uint32_t sr[KS / 32][32];
 #pragma unroll
       for (int c = 0; c < KS / 32; ++c) tmem_ld32(tl + cs + 32 * c, sr[c]);
@@ -634,8 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (need_mask) {
 #pragma unroll
         for (int e = 0; e < KS; ++e) {
-          const int key = key0 + e;
-          const bool keep = (key < kv_limit) & !((a.causal != 0) & (key > grow));
+          const bool keep = visible(grow, key0 + e, kv_limit, a.causal, window);
           p[e] = keep ? p[e] : 0.f;
         }
       }
@@ -652,9 +752,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float d0 = p[32 * c + 2 * e] * (__uint_as_float(dr[2 * e]) - Dr);
-          const float d1 = p[32 * c + 2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - Dr);
-          w[e] = pack_bf16(d0, d1);
+          // dS = P o (dP - D); with dropout dP = (dO V^T) Z / q.
+          const int ka = 32 * c + 2 * e;
+          float g0 = __uint_as_float(dr[2 * e]), g1 = __uint_as_float(dr[2 * e + 1]);
+          if constexpr (DROP) {
+            g0 = (km >> ka) & 1u ? g0 * a.drop_scale : 0.f;
+            g1 = (km >> (ka + 1)) & 1u ? g1 * a.drop_scale : 0.f;
+          }
+          w[e] = pack_bf16(p[ka] * (g0 - Dr), p[ka + 1] * (g1 - Dr));
         }
         // dS columns [16c, 16c+16) overwrite dP columns this thread has read.
         tmem_st16(tl + cdp + 16 * c, w);
@@ -729,34 +834,35 @@ cudaError_t set_smem(Kern k, int bytes, bool (&done)[64]) {
   return cudaSuccess;
 }
 
-template <int HD, int DH, int QS>
+template <int HD, int DH, int QS, bool DROP, bool MASKX>
 cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdArgs& a, cudaStream_t stream) {
   using C = KvCfg<HD, DH, QS>;
   static bool done[64] = {};
-  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<HD, DH, QS>, C::kSmemBytes, done);
+  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<HD, DH, QS, DROP, MASKX>, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(a.n_ktiles) * a.BH * C::kHalves;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dkdv_kernel<HD, DH, QS><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-      tmQ, tmK, tmV, tmdO, a);
+  fa_bwd_dkdv_kernel<HD, DH, QS, DROP, MASKX>
+      <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO, a);
   return cudaGetLastError();
 }
 
-template <int HD, int QT, int KS>
+template <int HD, int QT, int KS, bool DROP, bool MASKX>
 cudaError_t launch_dq_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdArgs& a,
                         cudaStream_t stream) {
   using C = QCfg<HD, QT, KS>;
   static bool done[64] = {};
-  cudaError_t e = set_smem(fa_bwd_dq_kernel<HD, QT, KS>, C::kSmemBytes, done);
+  cudaError_t e = set_smem(fa_bwd_dq_kernel<HD, QT, KS, DROP, MASKX>, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.n_qtiles + QT - 1) / QT) * a.BH;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dq_kernel<HD, QT, KS><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-      tmQ, tmK, tmV, tmdO, tmdQ, a);
+  fa_bwd_dq_kernel<HD, QT, KS, DROP, MASKX>
+      <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO,
+                                                                        tmdQ, a);
   return cudaGetLastError();
 }
 
@@ -768,7 +874,14 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tmQ, const CUtensorMap& tm
   switch (d) {
     case 64:
     case 128: return launch_bwd_dkdv_wide(d, tmQ, tmK, tmV, tmdO, a, stream);
-    case 256: return launch_dkdv_t<256, 128, 32>(tmQ, tmK, tmV, tmdO, a, stream);
+    case 256: {
+      const bool maskx = a.window >= 0 || a.bmask != nullptr;
+      if (a.drop_thr)
+        return maskx ? launch_dkdv_t<256, 128, 32, true, true>(tmQ, tmK, tmV, tmdO, a, stream)
+                     : launch_dkdv_t<256, 128, 32, true, false>(tmQ, tmK, tmV, tmdO, a, stream);
+      return maskx ? launch_dkdv_t<256, 128, 32, false, true>(tmQ, tmK, tmV, tmdO, a, stream)
+                   : launch_dkdv_t<256, 128, 32, false, false>(tmQ, tmK, tmV, tmdO, a, stream);
+    }
     default: return cudaErrorInvalidValue;
   }
 }
@@ -779,7 +892,14 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
   switch (d) {
     case 64:
     case 128: return launch_bwd_dq_wide(d, tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
-    case 256: return launch_dq_t<256, 1, 32>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    case 256: {
+      const bool maskx = a.window >= 0 || a.bmask != nullptr;
+      if (a.drop_thr)
+        return maskx ? launch_dq_t<256, 1, 32, true, true>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream)
+                     : launch_dq_t<256, 1, 32, true, false>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+      return maskx ? launch_dq_t<256, 1, 32, false, true>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream)
+                   : launch_dq_t<256, 1, 32, false, false>(tmQ, tmK, tmV, tmdO, tmdQ, a, stream);
+    }
     default: return cudaErrorInvalidValue;
   }
 }

@@ -94,4 +94,29 @@ __device__ __forceinline__ uint64_t keep64_transposed(uint32_t kw0, uint32_t i0,
   return m;
 }
 
+// The same for 32 consecutive queries i0 .. i0 + 31: every lane gets the 32
+// bits of its own key kw0 + lane (bit c <-> query i0 + c).  Lane l makes 4
+// generator calls -- key group l % 4 for the queries i0 + l / 4 + 8 t,
+// t = 0..3 -- and the bits are exchanged with 8 shuffles; all 32 lanes must
+// call this together.
+__device__ __forceinline__ uint32_t keep32_transposed(uint32_t kw0, uint32_t i0, uint32_t h,
+                                                      uint32_t b, uint32_t seed_lo,
+                                                      uint32_t seed_hi, uint32_t thr) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t g = lane & 3u, cl = lane >> 2;
+  uint32_t word = 0u;  // byte t: keys 8g..8g+7 for query cl + 8t
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    word |= keep8(kw0 + 8 * g, i0 + cl + 8 * t, h, b, seed_lo, seed_hi, thr) << (8 * t);
+  const uint32_t my_g = lane >> 3, my_bit = lane & 7u;
+  uint32_t m = 0;
+#pragma unroll
+  for (int c7 = 0; c7 < 8; ++c7) {
+    const uint32_t v = __shfl_sync(0xffffffffu, word, (c7 << 2) | static_cast<int>(my_g));
+#pragma unroll
+    for (int t = 0; t < 4; ++t) m |= ((v >> (8 * t + my_bit)) & 1u) << (c7 + 8 * t);
+  }
+  return m;
+}
+
 }  // namespace fa

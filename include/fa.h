@@ -97,8 +97,7 @@ fa_status fa_fwd_kvlen(const void* Q, const void* K, const void* V, void* O, flo
  * block mask leaves out are never computed: the kernels visit only the
  * blocks a query block (or key block) keeps.  A query that keeps no key gets
  * O = 0, L = -inf.
- * Errors: window < -1 gives FA_ERR_INVALID_ARG; window >= 0 or a block mask
- * with d = 256 gives FA_ERR_UNSUPPORTED.  Otherwise as fa_fwd_kvlen.
+ * Errors: window < -1 gives FA_ERR_INVALID_ARG.  Otherwise as fa_fwd_kvlen.
  */
 #define FA_MASK_BLOCK 128
 fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B,
@@ -119,8 +118,8 @@ fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, fl
  * kept iff value >= thr = floor(p * 65536), so q = (65536 - thr) / 65536 and
  * the scale is exactly 1/q.  The same (seed, p) gives the same decisions in
  * fa_bwd_dropout, which must be called with them.
- * Errors: p outside [0, 1) gives FA_ERR_INVALID_ARG; p > 0 with d = 256 gives
- * FA_ERR_UNSUPPORTED; otherwise as fa_fwd_masked.
+ * Errors: p outside [0, 1) gives FA_ERR_INVALID_ARG; otherwise as
+ * fa_fwd_masked.
  */
 fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* L, int B,
                          int H, int N, int d, float scale, int causal, const int32_t* kv_len,

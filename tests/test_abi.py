@@ -113,9 +113,12 @@ def test_masked_entry_points_validate_the_mask_terms(lib):
                                                    window, bm, fake, 1 << 20, null)
     for call in (fwd, bwd):
         assert call(64, -2, null) == 1          # window below -1
-        assert call(256, 8, null) == 2          # window on the d = 256 kernels
-        assert call(256, -1, fake) == 2         # block mask on the d = 256 kernels
         assert call(96, 8, null) == 2           # head dim
+    # d = 256 takes the window and block-mask terms: these calls get past the
+    # mask checks and stop at the short workspace
+    for window, bm in ((8, null), (-1, fake)):
+        assert lib.fa_bwd_masked(*([fake] * 9), 1, 1, 256, 256, f(0.1), 1, null, window, bm,
+                                 fake, 16, null) == 1
     assert lib.fa_fwd_masked(null, *([fake] * 4), 1, 1, 256, 64, f(0.1), 1, null, 4, null,
                              null) == 1
     assert lib.fa_bwd_masked(*([fake] * 9), 1, 1, 256, 64, f(0.1), 1, null, 4, null, fake, 16,
@@ -133,7 +136,10 @@ def test_dropout_entry_points_validate_the_probability(lib):
         assert call(64, -0.1) == 1
         assert call(64, 1.0) == 1
         assert call(64, float("nan")) == 1
-        assert call(256, 0.1) == 2      # dropout on the d = 256 kernels
+    # d = 256 takes dropout: the call gets past the probability check and stops
+    # at the short workspace
+    assert lib.fa_bwd_dropout(*([fake] * 9), 1, 1, 256, 256, f(0.1), 1, null, -1, null, f(0.1),
+                              u64(7), fake, 16, null) == 1
 
 
 def test_fp8_entry_point_validates_on_the_host(lib):

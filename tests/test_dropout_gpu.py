@@ -95,14 +95,14 @@ def test_keep_decisions_are_the_oracles():
                 assert np.array_equal(got[b, h], ref), (seed, b, h)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N,p", [(200, 0.1), (383, 0.5), (700, 0.25)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_dropout_parity(d, N, p, causal):
     check_full(H.Case(1600 + N, 2, 2, N, d), causal, p, SEED + N)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_dropout_with_key_padding_window_and_block_mask(d):
     N = 900
     case = H.Case(1701, 2, 2, N, d)
@@ -112,7 +112,7 @@ def test_dropout_with_key_padding_window_and_block_mask(d):
     check_full(case, False, 0.2, 99, bm=bm)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_zero_probability_is_the_plain_kernel_bitwise(d):
     import torch
     from exact_io_aware_40_gb300 import fa

@@ -61,7 +61,7 @@ def check_full(case, causal, window, bm):
     return o, L
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N,window", [(200, 0), (200, 1), (383, 127), (383, 128), (700, 300),
                                       (700, 1000)])
 @pytest.mark.parametrize("causal", [False, True])
@@ -69,14 +69,14 @@ def test_sliding_window(d, N, window, causal):
     check_full(H.Case(1100 + N, 1, 2, N, d), causal, window, None)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_sliding_window_with_key_padding(d):
     case = H.Case(1201, 3, 2, 640, d)
     case.set_kv_len([640, 300, 37])
     check_full(case, True, 200, None)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N,density,diagonal", [(300, 0.5, True), (1000, 0.3, True),
                                                 (1000, 0.4, False), (1153, 0.6, False)])
 @pytest.mark.parametrize("causal", [False, True])
@@ -86,7 +86,7 @@ def test_block_sparse(d, N, density, diagonal, causal):
     check_full(H.Case(1300 + N, 2, 2, N, d), causal, -1, bm)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_block_sparse_empty_rows_window_and_padding(d):
     N = 900
     nb = (N + 127) // 128
@@ -99,7 +99,7 @@ def test_block_sparse_empty_rows_window_and_padding(d):
     check_full(case, False, -1, bm)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_masks_that_change_nothing_change_nothing(d, causal):
     # An all-ones block mask, and a window wider than the sequence (with the

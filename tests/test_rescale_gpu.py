@@ -118,7 +118,7 @@ def test_rescale_other_scales(kind, factor, d, causal):
 
 
 @pytest.mark.parametrize("kind", ["ramp", "mid"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_rescale_window_and_block_mask(kind, d, causal):
     N = 1000
@@ -129,7 +129,7 @@ def test_rescale_window_and_block_mask(kind, d, causal):
 
 
 @pytest.mark.parametrize("kind", ["ramp", "mid"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_rescale_dropout(kind, d, causal):
     case = scenario_case(kind, 6300 + d, 1, 2, 1000, d)
