@@ -56,15 +56,23 @@ __device__ __forceinline__ void bar_sync_n(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// K-major operand of a tile whose 64-column atoms are `atom` bytes apart:
-// step k covers columns [16k, 16k+16) of d (atom k/4, 32 B per step).
-__device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t atom) {
-  return sdesc_sw128(base + (k >> 2) * atom + (k & 3) * 32, 16, 1024);
+// Descriptors of the K k-steps of a K-major operand whose 64-column atoms
+// are `atom` bytes apart: step k covers columns [16k, 16k+16) of d (atom k/4,
+// 32 B per step).
+template <int K>
+__device__ __forceinline__ void kmaj_steps(uint32_t base, uint32_t atom, uint64_t (&d)[K]) {
+  const uint64_t d0 = sdesc_sw128(base, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < K; ++k) d[k] = sdesc_add(d0, (k >> 2) * atom + (k & 3) * 32);
 }
-// MN-major operand (rows = reduction dim): step k covers rows [16k, 16k+16)
-// (two 8-row groups, SBO 1024 B); 64-column atoms are `atom` bytes apart (LBO).
-__device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t atom) {
-  return sdesc_sw128(base + k * 2048, atom, 1024);
+// The same for an MN-major operand (rows = reduction dim): step k covers rows
+// [16k, 16k+16) (two 8-row groups, SBO 1024 B); 64-column atoms are `atom`
+// bytes apart (LBO).
+template <int K>
+__device__ __forceinline__ void mnmaj_steps(uint32_t base, uint32_t atom, uint64_t (&d)[K]) {
+  const uint64_t d0 = sdesc_sw128(base, atom, 1024);
+#pragma unroll
+  for (int k = 0; k < K; ++k) d[k] = sdesc_add(d0, k * 2048);
 }
 
 // The steps of S rows (or keys) a CTA visits: the 128-blocks of a range from
@@ -281,21 +289,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t idS = idesc_bf16(kKeys, QS, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16(kKeys, DH, false, true);  // dV, dK
+      constexpr int kD = HD / 16, kQ = QS / 16;  // k-steps over d, over a query step
+      // Built once: descriptors of the resident K and V tiles.
+      uint64_t aK[kD], aV[kD];
+      kmaj_steps(sK, C::kKVAtom, aK);
+      kmaj_steps(sV, C::kKVAtom, aV);
       // S^T(i), dP^T(i) into warpgroup (i & 1)'s columns
       auto issue_s_dp = [&](int it) -> bool {
         const int st = it % C::kSt, x = it & 1;
         if (!mbar_wait(bar_qdo_full(st), (it / C::kSt) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t q = sQ + st * C::kQTile, g = sdO + st * C::kQTile;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + 2u * QS * x, kmaj(sK, k, C::kKVAtom), kmaj(q, k, C::kQAtom), idS,
-                 k > 0 ? 1u : 0u);
+        uint64_t b[kD];
+        kmaj_steps(sQ + st * C::kQTile, C::kQAtom, b);
+        mma_ss_k(tmem + 2u * QS * x, aK, b, idS, 0u);
         mma_commit(bar_s(x));
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + 2u * QS * x + QS, kmaj(sV, k, C::kKVAtom), kmaj(g, k, C::kQAtom), idS,
-                 k > 0 ? 1u : 0u);
+        kmaj_steps(sdO + st * C::kQTile, C::kQAtom, b);
+        mma_ss_k(tmem + 2u * QS * x + QS, aV, b, idS, 0u);
         mma_commit(bar_dp(x));
         return true;
       };
@@ -309,11 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pv = it - 1, y = pv & 1, st = pv % C::kSt;
           if (!(ok = mbar_wait(bar_ds(y), (pv >> 1) & 1, ab))) break;
           tc_fence_after();
+          {
+            uint32_t a[kQ];
+            uint64_t b[kQ];
 #pragma unroll
-          for (int k = 0; k < QS / 16; ++k)
-            mma_ts(tmem + C::kColdK, tmem + 2u * QS * y + QS + k * 8,
-                   mnmaj(sQ + st * C::kQTile + hatom * C::kQAtom, k, C::kQAtom), idKV,
-                   (pv > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kQ; ++k) a[k] = tmem + 2u * QS * y + QS + k * 8;
+            mnmaj_steps(sQ + st * C::kQTile + hatom * C::kQAtom, C::kQAtom, b);
+            mma_ts_k(tmem + C::kColdK, a, b, idKV, pv > 0 ? 1u : 0u);
+          }
           mma_commit(bar_qdo_empty(st));
           // S^T(it+1) overwrites P^T(it-1) and dP^T(it+1) overwrites dS^T(it-1):
           // dV(it-1) and dK(it-1) were issued first (MMAs execute in order).
@@ -323,11 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int x = it & 1, st = it % C::kSt;
           if (!(ok = mbar_wait(bar_p(x), (it >> 1) & 1, ab))) break;
           tc_fence_after();
+          uint32_t a[kQ];
+          uint64_t b[kQ];
 #pragma unroll
-          for (int k = 0; k < QS / 16; ++k)
-            mma_ts(tmem + C::kColdV, tmem + 2u * QS * x + k * 8,
-                   mnmaj(sdO + st * C::kQTile + hatom * C::kQAtom, k, C::kQAtom), idKV,
-                   (it > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kQ; ++k) a[k] = tmem + 2u * QS * x + k * 8;
+          mnmaj_steps(sdO + st * C::kQTile + hatom * C::kQAtom, C::kQAtom, b);
+          mma_ts_k(tmem + C::kColdV, a, b, idKV, it > 0 ? 1u : 0u);
         }
       }
       mma_commit(bar_final);
@@ -638,23 +651,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && T > 0) {
       constexpr uint32_t idS = idesc_bf16(kQRows, KS, false, false);  // S, dP
       constexpr uint32_t idQ = idesc_bf16(kQRows, HD, false, true);       // dQ
+      constexpr int kD = HD / 16, kK = KS / 16;  // k-steps over d, over a key step
       // S_x(j), dP_x(j) into block x's columns
       auto issue_s_dp = [&](int x, int j) -> bool {
         const int st = j % C::kSt;
         if (j == 0 && !mbar_wait(bar_qfull(x), 0, ab)) return false;
         if (!mbar_wait(bar_kvfull(st), (j / C::kSt) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t q = sQ + x * C::kQTile, g = sdO + x * C::kQTile;
-        const uint32_t k = sK + st * C::kKTile, v = sV + st * C::kKTile;
-#pragma unroll
-        for (int s = 0; s < HD / 16; ++s)
-          mma_ss(tmem + 2u * KS * x, kmaj(q, s, C::kQAtom), kmaj(k, s, C::kKAtom), idS,
-                 s > 0 ? 1u : 0u);
+        uint64_t a[kD], b[kD];
+        kmaj_steps(sQ + x * C::kQTile, C::kQAtom, a);
+        kmaj_steps(sK + st * C::kKTile, C::kKAtom, b);
+        mma_ss_k(tmem + 2u * KS * x, a, b, idS, 0u);
         mma_commit(bar_s(x));
-#pragma unroll
-        for (int s = 0; s < HD / 16; ++s)
-          mma_ss(tmem + 2u * KS * x + KS, kmaj(g, s, C::kQAtom), kmaj(v, s, C::kKAtom), idS,
-                 s > 0 ? 1u : 0u);
+        kmaj_steps(sdO + x * C::kQTile, C::kQAtom, a);
+        kmaj_steps(sV + st * C::kKTile, C::kKAtom, b);
+        mma_ss_k(tmem + 2u * KS * x + KS, a, b, idS, 0u);
         mma_commit(bar_dp(x));
         return true;
       };
@@ -669,10 +680,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar_ds(x), j & 1, ab))) break;
           tc_fence_after();
           // dQ_x += dS_x K_j (A = dS from TMEM, B = K_j MN-major)
+          {
+            uint32_t a[kK];
+            uint64_t b[kK];
 #pragma unroll
-          for (int s = 0; s < KS / 16; ++s)
-            mma_ts(tmem + C::kColdQ + static_cast<uint32_t>(HD) * x, tmem + 2u * KS * x + KS + s * 8,
-                   mnmaj(sK + st * C::kKTile, s, C::kKAtom), idQ, (j > 0 || s > 0) ? 1u : 0u);
+            for (int s = 0; s < kK; ++s) a[s] = tmem + 2u * KS * x + KS + s * 8;
+            mnmaj_steps(sK + st * C::kKTile, C::kKAtom, b);
+            mma_ts_k(tmem + C::kColdQ + static_cast<uint32_t>(HD) * x, a, b, idQ, j > 0 ? 1u : 0u);
+          }
           if (j == Tx - 1) mma_commit(bar_final(x));
           // the last reader of K_j, V_j releases the stage
           if (x == 1 || j >= TB) mma_commit(bar_kvempty(st));

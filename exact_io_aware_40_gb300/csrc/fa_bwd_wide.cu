@@ -56,15 +56,21 @@ __device__ __forceinline__ bool bar_and_w(int id, int nthreads, bool pred) {
 __device__ __forceinline__ void bar_sync_w(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-// K-major operand (128-row tile, 64-column atoms of 16 KB): step k covers
-// columns [16k, 16k+16) of d.
-__device__ __forceinline__ uint64_t kmaj128(uint32_t base, int k) {
-  return sdesc_sw128(base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+// Descriptors of the K k-steps of a K-major operand (128-row tile, 64-column
+// atoms of 16 KB): step k covers columns [16k, 16k+16) of d.
+template <int K>
+__device__ __forceinline__ void kmaj128_steps(uint32_t base, uint64_t (&d)[K]) {
+  const uint64_t d0 = sdesc_sw128(base, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < K; ++k) d[k] = sdesc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
 }
-// MN-major operand (128-row tile; rows = reduction dim): step k covers rows
-// [16k, 16k+16).
-__device__ __forceinline__ uint64_t mnmaj128(uint32_t base, int k) {
-  return sdesc_sw128(base + k * 2048, 16384, 1024);
+// The same for an MN-major operand (128-row tile; rows = reduction dim):
+// step k covers rows [16k, 16k+16).
+template <int K>
+__device__ __forceinline__ void mnmaj128_steps(uint32_t base, uint64_t (&d)[K]) {
+  const uint64_t d0 = sdesc_sw128(base, 16384, 1024);
+#pragma unroll
+  for (int k = 0; k < K; ++k) d[k] = sdesc_add(d0, k * 2048);
 }
 // TMEM column of k-step k (16 rows of the reduction dim) of a bf16 A operand
 // whose two 64-row halves sit at `lo` and `hi`.
@@ -249,18 +255,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t idS = idesc_bf16(kT, kT, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16(kT, HD, false, true);  // dV, dK
-      auto issue_s = [&](int it) {
-        const uint32_t q = sQ + (it % W::kSt) * W::kTile;
+      constexpr int kD = HD / 16, kQ = kT / 16;  // k-steps over d, over a query step
+      // Built once: descriptors of the resident K_j and V_j, TMEM addresses
+      // of the P^T and dS^T halves (A operands of dV and dK).
+      uint64_t aK[kD], aV[kD];
+      kmaj128_steps(sK, aK);
+      kmaj128_steps(sV, aV);
+      uint32_t tP[kQ], tdS[kQ];
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + C::kColS, kmaj128(sK, k), kmaj128(q, k), idS, k > 0 ? 1u : 0u);
+      for (int k = 0; k < kQ; ++k) {
+        tP[k] = tmem + split_col(C::kColS, C::kColS + 64, k);
+        tdS[k] = tmem + split_col(C::kColdP, C::kColdP + 64, k);
+      }
+      auto issue_s = [&](int it) {
+        uint64_t b[kD];
+        kmaj128_steps(sQ + (it % W::kSt) * W::kTile, b);
+        mma_ss_k(tmem + C::kColS, aK, b, idS, 0u);
         mma_commit(bar_s);
       };
       auto issue_dp = [&](int it) {
-        const uint32_t g = sdO + (it % W::kSt) * W::kTile;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + C::kColdP, kmaj128(sV, k), kmaj128(g, k), idS, k > 0 ? 1u : 0u);
+        uint64_t b[kD];
+        kmaj128_steps(sdO + (it % W::kSt) * W::kTile, b);
+        mma_ss_k(tmem + C::kColdP, aV, b, idS, 0u);
         mma_commit(bar_dp);
       };
       bool ok = mbar_wait(bar_kv, 0, ab) && mbar_wait(bar_qdo_full(0), 0, ab);
@@ -275,10 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dV += P^T dO_i (P^T halves at columns 0 and 64)
         if (!(ok = mbar_wait(bar_p, it & 1, ab))) break;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kT / 16; ++k)
-          mma_ts(tmem + C::kColdV, tmem + split_col(C::kColS, C::kColS + 64, k),
-                 mnmaj128(sdO + st * W::kTile, k), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        {
+          uint64_t b[kQ];
+          mnmaj128_steps(sdO + st * W::kTile, b);
+          mma_ts_k(tmem + C::kColdV, tP, b, idKV, it > 0 ? 1u : 0u);
+        }
         // S^T(i+1) overwrites P^T(i): the product above reads it first.
         if (more) {
           if (!(ok = mbar_wait(bar_qdo_full((it + 1) % W::kSt), ((it + 1) / W::kSt) & 1, ab)))
@@ -289,10 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dK += dS^T Q_i (dS^T halves at columns 128 and 192)
         if (!(ok = mbar_wait(bar_ds, it & 1, ab))) break;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kT / 16; ++k)
-          mma_ts(tmem + C::kColdK, tmem + split_col(C::kColdP, C::kColdP + 64, k),
-                 mnmaj128(sQ + st * W::kTile, k), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        {
+          uint64_t b[kQ];
+          mnmaj128_steps(sQ + st * W::kTile, b);
+          mma_ts_k(tmem + C::kColdK, tdS, b, idKV, it > 0 ? 1u : 0u);
+        }
         mma_commit(bar_qdo_empty(st));
         // dP^T(i+1) overwrites dS^T(i): dK above reads it first.
         if (more) issue_dp(it + 1);
@@ -613,15 +631,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && T > 0) {
       constexpr uint32_t idS = idesc_bf16(kT, kT, false, false);  // S, dP
       constexpr uint32_t idQ = idesc_bf16(kT, HD, false, true);   // dQ
+      constexpr int kD = HD / 16, kK = kT / 16;  // k-steps over d, over a key step
+      // Built once: descriptors of the resident Q and dO tiles.
+      uint64_t aQ[kD], adO[kD];
+      kmaj128_steps(sQ, aQ);
+      kmaj128_steps(sdO, adO);
       // S_j = Q K_j^T into buffer j & 1
       auto issue_s = [&](int j) -> bool {
         const int sk = j % C::kKSt;
         if (!mbar_wait(bar_kfull(sk), (j / C::kKSt) & 1, ab)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + C::kColS + 128u * (j & 1), kmaj128(sQ, k), kmaj128(sK + sk * W::kTile, k),
-                 idS, k > 0 ? 1u : 0u);
+        uint64_t b[kD];
+        kmaj128_steps(sK + sk * W::kTile, b);
+        mma_ss_k(tmem + C::kColS + 128u * (j & 1), aQ, b, idS, 0u);
         mma_commit(bar_s(j & 1));
         return true;
       };
@@ -630,10 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sv = j % C::kVSt;
         if (!mbar_wait(bar_vfull(sv), (j / C::kVSt) & 1, ab)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tmem + C::kColdP, kmaj128(sdO, k), kmaj128(sV + sv * W::kTile, k), idS,
-                 k > 0 ? 1u : 0u);
+        uint64_t b[kD];
+        kmaj128_steps(sV + sv * W::kTile, b);
+        mma_ss_k(tmem + C::kColdP, adO, b, idS, 0u);
         mma_commit(bar_dp);
         mma_commit(bar_vempty(sv));
         return true;
@@ -654,11 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // dQ += dS_j K_j (dS_j halves at columns 0 and 64 of S_j's buffer;
         // B = K_j MN-major)
-        const uint32_t sb = C::kColS + 128u * (j & 1);
+        {
+          const uint32_t sb = tmem + C::kColS + 128u * (j & 1);
+          uint32_t a[kK];
 #pragma unroll
-        for (int k = 0; k < kT / 16; ++k)
-          mma_ts(tmem + C::kColdQ, tmem + split_col(sb, sb + 64, k),
-                 mnmaj128(sK + sk * W::kTile, k), idQ, (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kK; ++k) a[k] = split_col(sb, sb + 64, k);
+          uint64_t b[kK];
+          mnmaj128_steps(sK + sk * W::kTile, b);
+          mma_ts_k(tmem + C::kColdQ, a, b, idQ, j > 0 ? 1u : 0u);
+        }
         if (j == T - 1) mma_commit(bar_final);
         mma_commit(bar_kempty(sk));
         // S_{j+2} overwrites dS_j: the product above reads it first (in order).

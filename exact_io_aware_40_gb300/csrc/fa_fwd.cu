@@ -246,20 +246,35 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
     if (lane == 0 && T > 0) {
       constexpr uint32_t idS = idesc_bf16(kBR, kBC, false, false);
       constexpr uint32_t idO = idesc_bf16(kBR, HD, false, true);
+      constexpr int kD = HD / 16, kC = kBC / 16;  // k-steps over d, over a key block
+      // K-major operands: step k covers columns [16k, 16k+16) of d, i.e. atom
+      // k/4, byte offset 32*(k%4) inside the 128-byte swizzled row.  The
+      // resident Q tile's descriptors are built once.
+      uint64_t aQ[kD];
+      {
+        const uint64_t d0 = sdesc_sw128(sQ, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < kD; ++k) aQ[k] = sdesc_add(d0, (k >> 2) * C::kAtomBytes + (k & 3) * 32);
+      }
       bool ok = mbar_wait(bar_q, 0, ab);
       auto issue_pv = [&](int jj) -> bool {
         const int bb = jj & 1, vs = jj % C::kVSt;
         if (!mbar_wait(bar_pfull0 + 8u * bb, (jj >> 1) & 1, ab)) return false;
         if (!mbar_wait(bar_vfull(vs), (jj / C::kVSt) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t vbase = sV + vs * C::kKVTile;
+        // B = V_j, MN-major: 16 key rows per step (two 8-row groups, SBO
+        // 1024 B); 64-column atoms of d are kKVAtom apart (LBO).  A = P_j
+        // from TMEM, 8 columns (16 bf16 keys) per step.
+        uint64_t b[kC];
+        uint32_t a[kC];
+        const uint64_t d0 = sdesc_sw128(sV + vs * C::kKVTile, C::kKVAtom, 1024);
+        const uint32_t pcol = tmem + s_col(bb);
 #pragma unroll
-        for (int k = 0; k < kBC / 16; ++k) {
-          // B = V_j, MN-major: 16 key rows per step (two 8-row groups, SBO
-          // 1024 B); 64-column atoms of d are kAtomBytes apart (LBO).
-          const uint64_t bdesc = sdesc_sw128(vbase + k * 2048, C::kKVAtom, 1024);
-          mma_ts(tmem + C::kColO, tmem + s_col(bb) + k * 8, bdesc, idO, (jj > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kC; ++k) {
+          b[k] = sdesc_add(d0, k * 2048);
+          a[k] = pcol + 8u * k;
         }
+        mma_ts_k(tmem + C::kColO, a, b, idO, jj > 0 ? 1u : 0u);
         mma_commit(bar_odone);
         mma_commit(bar_vempty(vs));
         return true;
@@ -269,15 +284,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
         if (j >= 2 && !mbar_wait(bar_odone, (j - 2) & 1, ab)) { ok = false; break; }
         if (!mbar_wait(bar_kfull(ks), (j / C::kKSt) & 1, ab)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kbase = sK + ks * C::kKVTile;
+        {
+          uint64_t b[kD];
+          const uint64_t d0 = sdesc_sw128(sK + ks * C::kKVTile, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          // K-major operands: step k covers columns [16k, 16k+16) of d, i.e.
-          // atom k/4, byte offset 32*(k%4) inside the 128-byte swizzled row.
-          const uint32_t qoff = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
-          const uint32_t koff = (k >> 2) * C::kKVAtom + (k & 3) * 32;
-          mma_ss(tmem + s_col(bb), sdesc_sw128(sQ + qoff, 16, 1024),
-                 sdesc_sw128(kbase + koff, 16, 1024), idS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < kD; ++k) b[k] = sdesc_add(d0, (k >> 2) * C::kKVAtom + (k & 3) * 32);
+          mma_ss_k(tmem + s_col(bb), aQ, b, idS, 0u);
         }
         mma_commit(bar_sfull0 + 8u * bb);
         mma_commit(bar_kempty(ks));

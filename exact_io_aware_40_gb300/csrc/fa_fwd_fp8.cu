@@ -81,10 +81,13 @@ __device__ __forceinline__ bool bar_and_128(int id, bool pred) {
   return r != 0;
 }
 
-// K-major 8-bit operand, 128-byte rows: step k covers elements [32k, 32k+32)
-// of the row, byte offset 32 k inside the swizzled row.
-__device__ __forceinline__ uint64_t kmaj8(uint32_t base, int k) {
-  return sdesc_sw128(base + 32u * k, 16, 1024);
+// Descriptors of the four k-steps of a K-major 8-bit operand with 128-byte
+// rows: step k covers elements [32k, 32k+32) of the row, byte offset 32 k
+// inside the swizzled row.
+__device__ __forceinline__ void kmaj8_steps(uint32_t base, uint64_t (&d)[4]) {
+  const uint64_t d0 = sdesc_sw128(base, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d[k] = sdesc_add(d0, 32u * k);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -193,17 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && T > 0) {
       constexpr uint32_t idS = idesc_e4m3(kBR, kBC);
       constexpr uint32_t idO = idesc_e4m3(kBR, kD);
+      static_assert(kD == 128 && kBC == 128, "four 32-element k-steps per product");
+      uint64_t aQ[4];  // the resident Q tile's descriptors, built once
+      kmaj8_steps(sQ, aQ);
       bool ok = mbar_wait(bar_q, 0, ab);
       auto issue_pv = [&](int jj) -> bool {
         const int bb = jj & 1, vs = jj % kSt;
         if (!mbar_wait(bar_pfull0 + 8u * bb, (jj >> 1) & 1, ab)) return false;
         if (!mbar_wait(bar_vfull(vs), (jj / kSt) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t pbase = sP + bb * kTile8, vbase = sV + vs * kTile8;
-#pragma unroll
-        for (int k = 0; k < kBC / 32; ++k)
-          mma_ss_f8(tmem + kColO, kmaj8(pbase, k), kmaj8(vbase, k), idO,
-                    (jj > 0 || k > 0) ? 1u : 0u);
+        uint64_t a[4], b[4];
+        kmaj8_steps(sP + bb * kTile8, a);
+        kmaj8_steps(sV + vs * kTile8, b);
+        mma_ss_f8_x4(tmem + kColO, a, b, idO, jj > 0 ? 1u : 0u);
         mma_commit(bar_odone);
         mma_commit(bar_vempty(vs));
         return true;
@@ -215,10 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= 2 && !mbar_wait(bar_odone, (j - 2) & 1, ab)) { ok = false; break; }
         if (!mbar_wait(bar_kfull(ks), (j / kSt) & 1, ab)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kbase = sK + ks * kTile8;
-#pragma unroll
-        for (int k = 0; k < kD / 32; ++k)
-          mma_ss_f8(tmem + s_col(bb), kmaj8(sQ, k), kmaj8(kbase, k), idS, k > 0 ? 1u : 0u);
+        {
+          uint64_t b[4];
+          kmaj8_steps(sK + ks * kTile8, b);
+          mma_ss_f8_x4(tmem + s_col(bb), aQ, b, idS, 0u);
+        }
         mma_commit(bar_sfull0 + 8u * bb);
         mma_commit(bar_kempty(ks));
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }

@@ -224,6 +224,74 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four or eight k-steps of one product in a single block, operands already
+// in registers: the issuing thread spends one instruction per MMA (the issue
+// thread shares its scheduler with the softmax warps, so every instruction
+// it executes between MMAs delays the tensor pipe).  The first k-step adds
+// to D when acc != 0, the later ones always.
+__device__ __forceinline__ void mma_ss_x4(uint32_t d, const uint64_t* a, const uint64_t* b,
+                                          uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 t, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, t;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc), "r"(idesc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_x4(uint32_t d, const uint32_t* a, const uint64_t* b,
+                                          uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 t, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %10, t;\n\t}" ::"r"(d),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc), "r"(idesc)
+      : "memory");
+}
+// Four k-steps of an e4m3 product (kind::f8f6f4), as mma_ss_x4.
+__device__ __forceinline__ void mma_ss_f8_x4(uint32_t d, const uint64_t* a, const uint64_t* b,
+                                             uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 t, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %10, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %10, t;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc), "r"(idesc)
+      : "memory");
+}
+// K k-steps of D (+)= A B^T, A and B from shared memory: blocks of four,
+// then single MMAs for the remainder.
+template <int K>
+__device__ __forceinline__ void mma_ss_k(uint32_t d, const uint64_t (&a)[K], const uint64_t (&b)[K],
+                                         uint32_t idesc, uint32_t acc) {
+#pragma unroll
+  for (int g = 0; g < K / 4; ++g) mma_ss_x4(d, a + 4 * g, b + 4 * g, idesc, g > 0 ? 1u : acc);
+#pragma unroll
+  for (int k = K / 4 * 4; k < K; ++k) mma_ss(d, a[k], b[k], idesc, k > 0 ? 1u : acc);
+}
+// The same with A read from tensor memory (one TMEM address per k-step).
+template <int K>
+__device__ __forceinline__ void mma_ts_k(uint32_t d, const uint32_t (&a)[K], const uint64_t (&b)[K],
+                                         uint32_t idesc, uint32_t acc) {
+#pragma unroll
+  for (int g = 0; g < K / 4; ++g) mma_ts_x4(d, a + 4 * g, b + 4 * g, idesc, g > 0 ? 1u : acc);
+#pragma unroll
+  for (int k = K / 4 * 4; k < K; ++k) mma_ts(d, a[k], b[k], idesc, k > 0 ? 1u : acc);
+}
+
 // Arrive once on `bar` when all previously issued tcgen05 async ops of this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -292,6 +360,15 @@ __device__ __forceinline__ void tmem_wait_st() {
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// The descriptor of the same operand `bytes` further on (a multiple of 16).
+// Shared-memory addresses stay below 2^18, so the 14-bit start-address field
+// (address >> 4) cannot carry into the next field and the add touches the low
+// word only: one integer add per k-step instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  const uint32_t lo = static_cast<uint32_t>(desc) + (bytes >> 4);
+  return (desc & 0xffffffff00000000ull) | lo;
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate:
