@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) {
         const int r = lane * 4 + e;
         const int q = q0 + r;
-        L2[r] = q < a.N ? a.L[rbase + q] * kLog2e : 0.f;
+        L2[r] = q < a.N ? -(a.L[rbase + q] * kLog2e) : 0.f;  // negated: the FMA adds it
         Dv[r] = q < a.N ? a.D[rbase + q] : 0.f;
       }
       mbar_arrive(bar_ld_full(st));
@@ -357,9 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + cs, sr[0]);
         tmem_ld32(tl + cs + 32, sr[1]);
         tmem_wait_ld();
+        // p = 2^(s^T scale log2e - L log2e) on packed fp32 pairs (the ring
+        // holds -L log2e).
+        const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
+        const uint64_t* nL2 = reinterpret_cast<const uint64_t*>(L2);
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          p[e] = ex2(fmaf(__uint_as_float(sr[e >> 5][e & 31]), a.scale_log2, -L2[e]));
+        for (int e = 0; e < 32; ++e) {
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e >> 4][(2 * e) & 31]),
+                                   __uint_as_float(sr[e >> 4][(2 * e + 1) & 31])),
+                           scl2, nL2[e]),
+                    t0, t1);
+          p[2 * e] = ex2(t0);
+          p[2 * e + 1] = ex2(t1);
+        }
         // One branch per step; inside, selects only (a branch per element in
         // the loop above costs more than the exponentials).
         if (need_mask) {
@@ -407,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t w[16];
           // dS^T = P^T o (dP^T - D); with dropout dP^T = (V dO^T) Z / q.
           auto ds_chunk = [&](auto drop) {
+            const uint64_t* Dv2 = reinterpret_cast<const uint64_t*>(Dv);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int qa = 32 * c + 2 * e;
@@ -415,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 g0 = (km >> qa) & 1u ? g0 * a.drop_scale : 0.f;
                 g1 = (km >> (qa + 1)) & 1u ? g1 * a.drop_scale : 0.f;
               }
-              w[e] = pack_bf16(p[qa] * (g0 - Dv[qa]), p[qa + 1] * (g1 - Dv[qa + 1]));
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(p[qa], p[qa + 1]), f2_sub(f2_pack(g0, g1), Dv2[qa >> 1])),
+                        d0, d1);
+              w[e] = pack_bf16(d0, d1);
             }
           };
           if constexpr (DROP)
@@ -730,11 +745,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tl + C::kColS + 128u * (j & 1) + 64u * x + 32, sr[1]);
       tmem_wait_ld();
       float p[64];
+      {
+        // p = 2^(s scale log2e - L log2e) on packed fp32 pairs
+        const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2), nL2 = f2_pack(-L2, -L2);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          p[32 * c + e] = ex2(fmaf(__uint_as_float(sr[c][e]), a.scale_log2, -L2));
+          for (int e = 0; e < 16; ++e) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
+                             scl2, nL2),
+                      t0, t1);
+            p[32 * c + 2 * e] = ex2(t0);
+            p[32 * c + 2 * e + 1] = ex2(t1);
+          }
         }
       }
       // One branch per step; inside, selects only.
@@ -761,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_dpfree);
       uint32_t w[32];
       // dS = P o (dP - D); with dropout dP = (dO V^T) Z / q.
+      const uint64_t Dr2 = f2_pack(Dr, Dr);
       auto ds_step = [&](auto drop) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -770,7 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             g0 = (km >> (2 * e)) & 1u ? g0 * a.drop_scale : 0.f;
             g1 = (km >> (2 * e + 1)) & 1u ? g1 * a.drop_scale : 0.f;
           }
-          w[e] = pack_bf16(p[2 * e] * (g0 - Dr), p[2 * e + 1] * (g1 - Dr));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p[2 * e], p[2 * e + 1]), f2_sub(f2_pack(g0, g1), Dr2)), d0, d1);
+          w[e] = pack_bf16(d0, d1);
         }
       };
       if constexpr (DROP)
