@@ -78,6 +78,20 @@ __device__ __forceinline__ uint32_t split_col(uint32_t lo, uint32_t hi, int k) {
   return k < 4 ? lo + 8u * k : hi + 8u * (k - 4);
 }
 
+// Stage and phase parity of a ring of S stages, advanced one slot at a time
+// (the MMA issuer keeps these instead of dividing a step count by S).
+template <int S>
+struct RingPos {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 template <int HD>
 struct WCfg {
   static constexpr int kAtoms = HD / 64;
@@ -267,15 +281,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tP[k] = tmem + split_col(C::kColS, C::kColS + 64, k);
         tdS[k] = tmem + split_col(C::kColdP, C::kColdP + 64, k);
       }
-      auto issue_s = [&](int it) {
+      // Q/dO stage of step it (cur) and of step it + 1 (nxt)
+      RingPos<W::kSt> cur, nxt;
+      auto issue_s = [&](int st) {
         uint64_t b[kD];
-        kmaj128_steps(sQ + (it % W::kSt) * W::kTile, b);
+        kmaj128_steps(sQ + st * W::kTile, b);
         mma_ss_k(tmem + C::kColS, aK, b, idS, 0u);
         mma_commit(bar_s);
       };
-      auto issue_dp = [&](int it) {
+      auto issue_dp = [&](int st) {
         uint64_t b[kD];
-        kmaj128_steps(sdO + (it % W::kSt) * W::kTile, b);
+        kmaj128_steps(sdO + st * W::kTile, b);
         mma_ss_k(tmem + C::kColdP, aV, b, idS, 0u);
         mma_commit(bar_dp);
       };
@@ -285,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_s(0);
         issue_dp(0);
       }
+      nxt.next();
       for (int it = 0; ok && it < n_iter; ++it) {
-        const int st = it % W::kSt;
+        const int st = cur.stage;
         const bool more = it + 1 < n_iter;
         // dV += P^T dO_i (P^T halves at columns 0 and 64)
         if (!(ok = mbar_wait(bar_p, it & 1, ab))) break;
@@ -298,10 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // S^T(i+1) overwrites P^T(i): the product above reads it first.
         if (more) {
-          if (!(ok = mbar_wait(bar_qdo_full((it + 1) % W::kSt), ((it + 1) / W::kSt) & 1, ab)))
-            break;
+          if (!(ok = mbar_wait(bar_qdo_full(nxt.stage), nxt.phase, ab))) break;
           tc_fence_after();
-          issue_s(it + 1);
+          issue_s(nxt.stage);
         }
         // dK += dS^T Q_i (dS^T halves at columns 128 and 192)
         if (!(ok = mbar_wait(bar_ds, it & 1, ab))) break;
@@ -313,7 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar_qdo_empty(st));
         // dP^T(i+1) overwrites dS^T(i): dK above reads it first.
-        if (more) issue_dp(it + 1);
+        if (more) issue_dp(nxt.stage);
+        cur.next();
+        nxt.next();
       }
       mma_commit(bar_final);
       mma_commit(bar_drain);
@@ -651,40 +669,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t aQ[kD], adO[kD];
       kmaj128_steps(sQ, aQ);
       kmaj128_steps(sdO, adO);
+      RingPos<C::kKSt> ks, kq;  // K stages of the next S product and of dQ_j
+      RingPos<C::kVSt> vs;      // V stage of the next dP product
       // S_j = Q K_j^T into buffer j & 1
       auto issue_s = [&](int j) -> bool {
-        const int sk = j % C::kKSt;
-        if (!mbar_wait(bar_kfull(sk), (j / C::kKSt) & 1, ab)) return false;
+        if (!mbar_wait(bar_kfull(ks.stage), ks.phase, ab)) return false;
         tc_fence_after();
         uint64_t b[kD];
-        kmaj128_steps(sK + sk * W::kTile, b);
+        kmaj128_steps(sK + ks.stage * W::kTile, b);
         mma_ss_k(tmem + C::kColS + 128u * (j & 1), aQ, b, idS, 0u);
         mma_commit(bar_s(j & 1));
+        ks.next();
         return true;
       };
       // dP_j = dO V_j^T; V_j's stage is free again once it completes.
-      auto issue_dp = [&](int j) -> bool {
-        const int sv = j % C::kVSt;
-        if (!mbar_wait(bar_vfull(sv), (j / C::kVSt) & 1, ab)) return false;
+      auto issue_dp = [&]() -> bool {
+        if (!mbar_wait(bar_vfull(vs.stage), vs.phase, ab)) return false;
         tc_fence_after();
         uint64_t b[kD];
-        kmaj128_steps(sV + sv * W::kTile, b);
+        kmaj128_steps(sV + vs.stage * W::kTile, b);
         mma_ss_k(tmem + C::kColdP, adO, b, idS, 0u);
         mma_commit(bar_dp);
-        mma_commit(bar_vempty(sv));
+        mma_commit(bar_vempty(vs.stage));
+        vs.next();
         return true;
       };
       bool ok = mbar_wait(bar_q, 0, ab);
       if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp(0);
+      if (ok) ok = issue_dp();
       if (ok && T > 1) ok = issue_s(1);
       for (int j = 0; ok && j < T; ++j) {
-        const int sk = j % C::kKSt;
         // dP_{j+1} as soon as the warpgroups hold dP_j in registers.
         if (j + 1 < T) {
           if (!(ok = mbar_wait(bar_dpfree, j & 1, ab))) break;
           tc_fence_after();
-          if (!(ok = issue_dp(j + 1))) break;
+          if (!(ok = issue_dp())) break;
         }
         if (!(ok = mbar_wait(bar_ds, j & 1, ab))) break;
         tc_fence_after();
@@ -696,11 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kK; ++k) a[k] = split_col(sb, sb + 64, k);
           uint64_t b[kK];
-          mnmaj128_steps(sK + sk * W::kTile, b);
+          mnmaj128_steps(sK + kq.stage * W::kTile, b);
           mma_ts_k(tmem + C::kColdQ, a, b, idQ, j > 0 ? 1u : 0u);
         }
         if (j == T - 1) mma_commit(bar_final);
-        mma_commit(bar_kempty(sk));
+        mma_commit(bar_kempty(kq.stage));
+        kq.next();
         // S_{j+2} overwrites dS_j: the product above reads it first (in order).
         if (j + 2 < T && !(ok = issue_s(j + 2))) break;
       }
