@@ -60,11 +60,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
 # launches), valid only while the kernel source hashes to the recorded digest.
 # Capture: H=8 (same kernels, half the heads, inputs still larger than L2),
-# 135.3 MB read + 32.1 MB written (causal 0) and 155.8 + 22.7 MB (causal 1;
+# 135.3 MB read + 31.4 MB written (causal 0) and 154.5 + 26.2 MB (causal 1;
 # the grouped CTA order of a causal launch re-reads some Q, dO blocks);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "2b0cd8332471b828852456b7901d84cf8dd51dd80f74e7c04cf6d771b6146425",
-                    "bytes_per_launch": 2 * (167.49e6 + 178.53e6) / 2}
+BWD_DKDV_TRAFFIC = {"sha256": "5f30f8a59f4d67236f9cfcb10a1aec4e7f54742ee6d019b12360f998749c2801",
+                    "bytes_per_launch": 2 * (166.68e6 + 180.71e6) / 2}
 
 
 def pairs(causal, b=None, h=None, n=None):
