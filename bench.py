@@ -63,7 +63,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # 135.3 MB read + 31.4 MB written (causal 0) and 154.5 + 26.2 MB (causal 1;
 # the grouped CTA order of a causal launch re-reads some Q, dO blocks);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "5f30f8a59f4d67236f9cfcb10a1aec4e7f54742ee6d019b12360f998749c2801",
+BWD_DKDV_TRAFFIC = {"sha256": "9251163979c148a0951c35151a9a09fb8c992c4dbf128af7288bae0f7c01ef7e",
                     "bytes_per_launch": 2 * (166.68e6 + 180.71e6) / 2}
 
 

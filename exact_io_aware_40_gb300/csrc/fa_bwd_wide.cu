@@ -3,12 +3,11 @@
 // Same method and formulas as fa_bwd.cu (P recomputed from L; dV = P^T dO,
 // dP = dO V^T, dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q; fmread.com
 // summary, section 三.2 "反向传播优化"), organised so that every tcgen05 product
-// is 128 wide (M = 128, N = 128): a product with N = 64 and both operands in
-// shared memory needs 192 B/clock of shared-memory bandwidth at full tensor
-// rate, more than an SM has, so it runs at two thirds of the rate at best;
-// N = 128 needs 128 B/clock (operands in shared memory) or 64 B/clock (A in
-// TMEM).  Each 128-wide step is split by columns between two softmax
-// warpgroups, so both work on every step in parallel:
+// is 128 wide (M = 128, N = 128): an M = 128 product instruction takes at
+// least about 45 clocks, so one with N = 64 runs at two thirds of the tensor
+// rate whatever its operands' source, while N = 128 runs at the full rate
+// (64 clocks per 16-deep k-step).  Each 128-wide step is split by columns
+// between two softmax warpgroups, so both work on every step in parallel:
 //
 // fa_bwd_dkdv_wide_kernel -- one CTA per 128-key block j, 128-row query steps
 //   i.  TMEM: S^T 0-127, dP^T 128-255 (keys on lanes, queries on columns), dV
