@@ -111,8 +111,8 @@ struct KvW {
   static constexpr int kLdSt = 4;                               // L, D ring depth
   static constexpr int kOffLD = kOffdO + W::kSt * W::kTile;     // kLdSt x (L2[128], D[128])
   static constexpr int kOffBar = kOffLD + kLdSt * 1024;
-  // kv, qdo_full[], qdo_empty[], ld_full[4], ld_empty[4], s, dp, p, ds, final, drain
-  static constexpr int kNumBar = 1 + 2 * W::kSt + 2 * kLdSt + 6;
+  // k, qdo_full[], qdo_empty[], ld_full[4], ld_empty[4], s, dp, p, ds, final, drain, v
+  static constexpr int kNumBar = 1 + 2 * W::kSt + 2 * kLdSt + 7;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -145,6 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_s = bar0 + 8u * (1 + 2 * W::kSt + 2 * C::kLdSt);
   const uint32_t bar_dp = bar_s + 8, bar_p = bar_s + 16, bar_ds = bar_s + 24;
   const uint32_t bar_final = bar_s + 32, bar_drain = bar_s + 40;
+  // K_j and V_j land on separate barriers: the first S^T needs K_j and Q_0
+  // only, so those are loaded first and V_j after them.
+  const uint32_t bar_v = bar_s + 48;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
+    mbar_init(bar_v, 1);
     for (int s = 0; s < W::kSt; ++s) {
       mbar_init(bar_qdo_full(s), 1);
       mbar_init(bar_qdo_empty(s), 1);
@@ -209,11 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         pol_kv = policy_evict_first();
         pol_q = policy_evict_last();  // Q_i, dO_i are re-read by every key block
-        mbar_arrive_expect_tx(bar_kv, 2 * W::kTile);
-        for (int c = 0; c < W::kAtoms; ++c) {
+        mbar_arrive_expect_tx(bar_kv, W::kTile);
+        for (int c = 0; c < W::kAtoms; ++c)
           tma_load_3d(sK + c * 16384, &tmK, c * 64, k0, bh, bar_kv, pol_kv);
-          tma_load_3d(sV + c * 16384, &tmV, c * 64, k0, bh, bar_kv, pol_kv);
-        }
       }
       int last[W::kSt];
       for (int t = 0; t < W::kSt; ++t) last[t] = -1;
@@ -232,11 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sdO + st * W::kTile + c * 16384, &tmdO, c * 64, q0, bh,
                         bar_qdo_full(st), pol_q);
           }
+          if (it == 0) {
+            mbar_arrive_expect_tx(bar_v, W::kTile);
+            for (int c = 0; c < W::kAtoms; ++c)
+              tma_load_3d(sV + c * 16384, &tmV, c * 64, k0, bh, bar_v, pol_kv);
+          }
         }
         last[st] = it;
       }
       if (lane == 0 && *abort_flag) {
         mbar_wait_drain(bar_kv, 0);
+        mbar_wait_drain(bar_v, 0);
         for (int s = 0; s < W::kSt; ++s)
           if (last[s] >= 0) mbar_wait_drain(bar_qdo_full(s), (last[s] / W::kSt) & 1);
       }
@@ -298,6 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_s(0);
+      }
+      if (ok && (ok = mbar_wait(bar_v, 0, ab))) {
+        tc_fence_after();
         issue_dp(0);
       }
       nxt.next();
@@ -527,8 +538,9 @@ struct QW {
   static constexpr int kOffK = 2 * W::kTile;
   static constexpr int kOffV = kOffK + kKSt * W::kTile;
   static constexpr int kOffBar = kOffV + kVSt * W::kTile;
-  // q_full, k_full[], k_empty[], v_full[], v_empty[], s[2], dp, ds, final, drain, dp_free
-  static constexpr int kNumBar = 1 + 2 * kKSt + 2 * kVSt + 7;
+  // q_full, k_full[], k_empty[], v_full[], v_empty[], s[2], dp, ds, final, drain, dp_free,
+  // do_full
+  static constexpr int kNumBar = 1 + 2 * kKSt + 2 * kVSt + 8;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -561,6 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_s = [&](int b2) { return barx + 8u * b2; };
   const uint32_t bar_dp = barx + 16, bar_ds = barx + 24, bar_final = barx + 32, bar_drain = barx + 40;
   const uint32_t bar_dpfree = barx + 48;
+  // Q and dO land on separate barriers: the first S needs Q and K_0 only, so
+  // those are loaded first and dO, V_0 after them.
+  const uint32_t bar_do = barx + 56;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -587,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
+    mbar_init(bar_do, 1);
     for (int s = 0; s < C::kKSt; ++s) {
       mbar_init(bar_kfull(s), 1);
       mbar_init(bar_kempty(s), 1);
@@ -626,11 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && T > 0) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(bar_q, 2 * W::kTile);
-      for (int c = 0; c < W::kAtoms; ++c) {
+      mbar_arrive_expect_tx(bar_q, W::kTile);
+      for (int c = 0; c < W::kAtoms; ++c)
         tma_load_3d(sQ + c * 16384, &tmQ, c * 64, q0, bh, bar_q, pol_q);
-        tma_load_3d(sdO + c * 16384, &tmdO, c * 64, q0, bh, bar_q, pol_q);
-      }
       int lastk[C::kKSt], lastv[C::kVSt];
       for (int s = 0; s < C::kKSt; ++s) lastk[s] = -1;
       for (int s = 0; s < C::kVSt; ++s) lastv[s] = -1;
@@ -643,6 +657,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sK + sk * W::kTile + c * 16384, &tmK, c * 64, kb * kT, bh, bar_kfull(sk),
                       pol_kv);
         lastk[sk] = j;
+        if (j == 0) {
+          mbar_arrive_expect_tx(bar_do, W::kTile);
+          for (int c = 0; c < W::kAtoms; ++c)
+            tma_load_3d(sdO + c * 16384, &tmdO, c * 64, q0, bh, bar_do, pol_q);
+        }
         if (j >= C::kVSt && !mbar_wait(bar_vempty(sv), ((j / C::kVSt) & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(bar_vfull(sv), W::kTile);
         for (int c = 0; c < W::kAtoms; ++c)
@@ -652,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {
         mbar_wait_drain(bar_q, 0);
+        mbar_wait_drain(bar_do, 0);
         for (int s = 0; s < C::kKSt; ++s)
           if (lastk[s] >= 0) mbar_wait_drain(bar_kfull(s), (lastk[s] / C::kKSt) & 1);
         for (int s = 0; s < C::kVSt; ++s)
@@ -695,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = mbar_wait(bar_q, 0, ab);
       if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp();
+      if (ok) ok = mbar_wait(bar_do, 0, ab) && issue_dp();
       if (ok && T > 1) ok = issue_s(1);
       for (int j = 0; ok && j < T; ++j) {
         // dP_{j+1} as soon as the warpgroups hold dP_j in registers.
