@@ -60,11 +60,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # dram__bytes_write.sum from one ncu capture, mean of the causal and non-causal
 # launches), valid only while the kernel source hashes to the recorded digest.
 # Capture: H=8 (same kernels, half the heads, inputs still larger than L2),
-# 135.3 MB read + 31.4 MB written (causal 0) and 154.5 + 26.2 MB (causal 1;
+# 135.4 MB read + 31.6 MB written (causal 0) and 154.0 + 22.7 MB (causal 1;
 # the grouped CTA order of a causal launch re-reads some Q, dO blocks);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "9251163979c148a0951c35151a9a09fb8c992c4dbf128af7288bae0f7c01ef7e",
-                    "bytes_per_launch": 2 * (166.68e6 + 180.71e6) / 2}
+BWD_DKDV_TRAFFIC = {"sha256": "f45e0568a6328c0321b049f3206abb278f06caec3976a9f3b534561889f06654",
+                    "bytes_per_launch": 2 * (166.98e6 + 176.73e6) / 2}
 
 
 def pairs(causal, b=None, h=None, n=None):
