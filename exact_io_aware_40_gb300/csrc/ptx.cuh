@@ -357,7 +357,8 @@ __device__ __forceinline__ void tmem_wait_st() {
 //   bits 32-45 stride byte offset >> 4 bits 46-48 fixed 0b001
 //   bits 49-51 base offset (0: atoms are 1024-byte aligned)
 //   bits 61-63 swizzle mode (2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+__host__ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
+                                                       uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
@@ -366,7 +367,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 // Shared-memory addresses stay below 2^18, so the 14-bit start-address field
 // (address >> 4) cannot carry into the next field and the add touches the low
 // word only: one integer add per k-step instead of rebuilding the descriptor.
-__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+__host__ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
   const uint32_t lo = static_cast<uint32_t>(desc) + (bytes >> 4);
   return (desc & 0xffffffff00000000ull) | lo;
 }
