@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < QS / 32; ++e) {
           const int r = lane * (QS / 32) + e;
           const int q = q0 + r;
-          L2[r] = q < a.N ? a.L[rbase + q] * kLog2e : 0.f;
+          L2[r] = q < a.N ? -(a.L[rbase + q] * kLog2e) : 0.f;  // negated: the FMA adds it
           Dv[r] = q < a.N ? a.D[rbase + q] : 0.f;
         }
         mbar_arrive(bar_ld_full(st));
@@ -390,10 +390,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + cs + 32 * c, sr);
         tmem_wait_ld();
         uint32_t w[16];
+        // p = 2^(s^T scale log2e - L log2e) on packed fp32 pairs (the ring
+        // holds -L log2e)
+        const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2);
+        const uint64_t* nL2 = reinterpret_cast<const uint64_t*>(L2 + 32 * c);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int qa = 32 * c + e;
-          p[qa] = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -L2[qa]));
+        for (int e = 0; e < 16; ++e) {
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
+                           scl2, nL2[e]),
+                    t0, t1);
+          p[32 * c + 2 * e] = ex2(t0);
+          p[32 * c + 2 * e + 1] = ex2(t1);
         }
         // One branch per chunk; inside, selects only (a branch per element
         // in the loop above costs more than the exponentials).
@@ -442,8 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             g0 = (km >> qa) & 1u ? g0 * a.drop_scale : 0.f;
             g1 = (km >> (qa + 1)) & 1u ? g1 * a.drop_scale : 0.f;
           }
-          const float d0 = p[qa] * (g0 - Dv[qa]);
-          const float d1 = p[qa + 1] * (g1 - Dv[qa + 1]);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p[qa], p[qa + 1]),
+                           f2_sub(f2_pack(g0, g1), reinterpret_cast<const uint64_t*>(Dv)[qa >> 1])),
+                    d0, d1);
           w[e] = pack_bf16(d0, d1);
         }
         // dS^T columns [16c, 16c+16) overwrite dP^T columns this thread has read.
@@ -739,11 +749,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < KS / 32; ++c) tmem_ld32(tl + cs + 32 * c, sr[c]);
       tmem_wait_ld();
       float p[KS];
+      {
+        // p = 2^(s scale log2e - L log2e) on packed fp32 pairs
+        const uint64_t scl2 = f2_pack(a.scale_log2, a.scale_log2), nL2 = f2_pack(-L2, -L2);
 #pragma unroll
-      for (int c = 0; c < KS / 32; ++c) {
+        for (int c = 0; c < KS / 32; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          p[32 * c + e] = ex2(fmaf(__uint_as_float(sr[c][e]), a.scale_log2, -L2));
+          for (int e = 0; e < 16; ++e) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
+                             scl2, nL2),
+                      t0, t1);
+            p[32 * c + 2 * e] = ex2(t0);
+            p[32 * c + 2 * e + 1] = ex2(t1);
+          }
         }
       }
       // One branch per step; inside, selects only.
@@ -774,7 +793,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             g0 = (km >> ka) & 1u ? g0 * a.drop_scale : 0.f;
             g1 = (km >> (ka + 1)) & 1u ? g1 * a.drop_scale : 0.f;
           }
-          w[e] = pack_bf16(p[ka] * (g0 - Dr), p[ka + 1] * (g1 - Dr));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p[ka], p[ka + 1]), f2_sub(f2_pack(g0, g1), f2_pack(Dr, Dr))),
+                    d0, d1);
+          w[e] = pack_bf16(d0, d1);
         }
         // dS columns [16c, 16c+16) overwrite dP columns this thread has read.
         tmem_st16(tl + cdp + 16 * c, w);
