@@ -63,7 +63,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # 135.4 MB read + 31.6 MB written (causal 0) and 154.0 + 22.7 MB (causal 1;
 # the grouped CTA order of a causal launch re-reads some Q, dO blocks);
 # per-head traffic is identical, so a 16-head launch moves twice that.
-BWD_DKDV_TRAFFIC = {"sha256": "c5474dd69a69d23dbf8c36d332f46a279c6c6d486e7504e469a8630d9bfba634",
+BWD_DKDV_TRAFFIC = {"sha256": "4cc69bb8cf7f9ac1ce5be439e3362c9a73c49ee4158a93cab10cbd882a4b1505",
                     "bytes_per_launch": 2 * (166.98e6 + 176.73e6) / 2}
 
 

@@ -294,10 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t aK[kD], aV[kD];
       kmaj_steps(sK, C::kKVAtom, aK);
       kmaj_steps(sV, C::kKVAtom, aV);
-      // S^T(i), dP^T(i) into warpgroup (i & 1)'s columns
+      // S^T(i), dP^T(i) into warpgroup (i & 1)'s columns; sp is the Q/dO
+      // stage of the next step issued (one call per step, in order).
+      RingPos<C::kSt> sp;
       auto issue_s_dp = [&](int it) -> bool {
-        const int st = it % C::kSt, x = it & 1;
-        if (!mbar_wait(bar_qdo_full(st), (it / C::kSt) & 1, ab)) return false;
+        const int st = sp.stage, x = it & 1;
+        if (!mbar_wait(bar_qdo_full(st), sp.phase, ab)) return false;
+        sp.next();
         tc_fence_after();
         uint64_t b[kD];
         kmaj_steps(sQ + st * C::kQTile, C::kQAtom, b);
@@ -313,9 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && n_iter > 1) ok = issue_s_dp(1);
       // Step it: dK(it-1), then S^T/dP^T(it+1) into the columns step it-1 has
       // released, then dV(it).
+      int st_cur = 0, st_prev = 0;  // Q/dO stages of steps it and it - 1
       for (int it = 0; ok && it <= n_iter; ++it) {
         if (it >= 1) {
-          const int pv = it - 1, y = pv & 1, st = pv % C::kSt;
+          const int pv = it - 1, y = pv & 1, st = st_prev;
           if (!(ok = mbar_wait(bar_ds(y), (pv >> 1) & 1, ab))) break;
           tc_fence_after();
           {
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it + 1 < n_iter && !(ok = issue_s_dp(it + 1))) break;
         }
         if (it < n_iter) {
-          const int x = it & 1, st = it % C::kSt;
+          const int x = it & 1, st = st_cur;
           if (!(ok = mbar_wait(bar_p(x), (it >> 1) & 1, ab))) break;
           tc_fence_after();
           uint32_t a[kQ];
@@ -342,6 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mnmaj_steps(sdO + st * C::kQTile + hatom * C::kQAtom, C::kQAtom, b);
           mma_ts_k(tmem + C::kColdV, a, b, idKV, it > 0 ? 1u : 0u);
         }
+        st_prev = st_cur;
+        st_cur = st_cur + 1 == C::kSt ? 0 : st_cur + 1;
       }
       mma_commit(bar_final);
       mma_commit(bar_drain);
@@ -663,10 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idQ = idesc_bf16(kQRows, HD, false, true);       // dQ
       constexpr int kD = HD / 16, kK = KS / 16;  // k-steps over d, over a key step
       // S_x(j), dP_x(j) into block x's columns
-      auto issue_s_dp = [&](int x, int j) -> bool {
-        const int st = j % C::kSt;
+      // The K/V stage and phase of step j come with the call.
+      auto issue_s_dp = [&](int x, int j, int st, uint32_t ph) -> bool {
         if (j == 0 && !mbar_wait(bar_qfull(x), 0, ab)) return false;
-        if (!mbar_wait(bar_kvfull(st), (j / C::kSt) & 1, ab)) return false;
+        if (!mbar_wait(bar_kvfull(st), ph, ab)) return false;
         tc_fence_after();
         uint64_t a[kD], b[kD];
         kmaj_steps(sQ + x * C::kQTile, C::kQAtom, a);
@@ -680,10 +686,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool ok = true;
-      if (TA > 0) ok = issue_s_dp(0, 0);
-      if (ok && TB > 0) ok = issue_s_dp(1, 0);
-      for (int j = 0; ok && j < T; ++j) {
-        const int st = j % C::kSt;
+      if (TA > 0) ok = issue_s_dp(0, 0, 0, 0u);
+      if (ok && TB > 0) ok = issue_s_dp(1, 0, 0, 0u);
+      RingPos<C::kSt> cur, nxt;  // K/V stages of steps j and j + 1
+      nxt.next();
+      for (int j = 0; ok && j < T; ++j, cur.next(), nxt.next()) {
+        const int st = cur.stage;
         for (int x = 0; x < 2 && ok; ++x) {
           const int Tx = x == 0 ? TA : TB;
           if (j >= Tx) continue;
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (x == 1 || j >= TB) mma_commit(bar_kvempty(st));
           // S_x(j+1) and dP_x(j+1) overwrite S_x(j) (read) and dS_x(j) (read by
           // the product just issued: MMAs execute in order).
-          if (j + 1 < Tx) ok = issue_s_dp(x, j + 1);
+          if (j + 1 < Tx) ok = issue_s_dp(x, j + 1, nxt.stage, nxt.phase);
         }
       }
       mma_commit(bar_drain);

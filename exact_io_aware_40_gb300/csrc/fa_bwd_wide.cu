@@ -77,20 +77,6 @@ __device__ __forceinline__ uint32_t split_col(uint32_t lo, uint32_t hi, int k) {
   return k < 4 ? lo + 8u * k : hi + 8u * (k - 4);
 }
 
-// Stage and phase parity of a ring of S stages, advanced one slot at a time
-// (the MMA issuer keeps these instead of dividing a step count by S).
-template <int S>
-struct RingPos {
-  int stage = 0;
-  uint32_t phase = 0;
-  __device__ __forceinline__ void next() {
-    if (++stage == S) {
-      stage = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 template <int HD>
 struct WCfg {
   static constexpr int kAtoms = HD / 64;

@@ -351,6 +351,20 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Stage and phase parity of a ring of S stages, advanced one slot at a time
+// (the MMA issuer keeps these instead of dividing a step count by S).
+template <int S>
+struct RingPos {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
